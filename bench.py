@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""Benchmark of one DDP gradient-synchronisation step over p simulated replicas
+held in one GPU's memory.
+
+A step is one pass of the whole hot path on the workload's synthetic
+gradients: bucket assignment (host), the per-forward coalesced broadcast of the
+model's buffers from replica 0, then for every bucket in order flatten ->
+ring all-reduce (fused one-pass kernel by default) and finally unflatten of
+every bucket back into the gradients.
+
+Default workload: the ResNet-50-shaped gradient set (161 fp32 tensors, 25.6M
+parameters) on p = 8 replicas, 1 MiB first bucket / 25 MiB buckets, averaged
+by 1/8, plus the broadcast of its 159 BatchNorm buffers.
+
+Prints ONE JSON line (rank 0). value = algorithmic bytes of all the step's ops
+(all-reduce 2pM, flatten 2pM, unflatten 2pM, broadcast p * buffer bytes) over
+the device-timed step, in GB/s, summed over ranks. --impl reference times the
+CPU oracle instead (on a bounded sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "simulated ring-allreduce HBM GB/s (frac of GB300 peak) vs bucket size, rank count"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD_TEXT = {
+    "resnet50": ("ResNet-50-shaped gradient set: 161 fp32 tensors (25,557,032 params), p=8 simulated "
+                 "replicas, reversed-registration buckets with 1 MiB first / 25 MiB cap, average by 1/8; "
+                 "plus per-forward coalesced broadcast of the 159 BatchNorm buffers from replica 0"),
+    "gpt2_small": ("GPT-2-small-shaped gradient set: 148 fp32 tensors (124,439,808 params), p=8, 25 MiB "
+                   "buckets, divide once by the global token count"),
+    "llama_1b": ("Llama-style 1B gradient set: 147 bf16 tensors (1,204,881,408 params), p=8, 25 MiB "
+                 "buckets, fp32 accumulate, average by 1/8; plus per-forward broadcast of 64 fp32 buffers"),
+    "tiny": "ten odd-sized fp32 tensors (277,421 elements), p=4, 16 KiB / 256 KiB buckets, average by 1/4",
+}
+
+# DRAM traffic of the fused all-reduce kernel from an ncu capture (bytes per
+# launch per algorithmic byte), valid only while the kernel source is unchanged.
+NCU_TRAFFIC = {"kernel_sha256": None, "dram_bytes_per_algorithmic_byte": None}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="resnet50", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--algo", default="fused", choices=["fused", "ldst", "ring_steps"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--sweep", action="store_true", help="message-size / rank-count sweep, one line per point")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------- ranks
+class Ranks:
+    """One process per GPU (torchrun); independent replicas, no data-path collective.
+    The process group serves the barrier and the max over ranks of the timings."""
+
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            import torch
+            if torch.cuda.is_available():
+                self.dist.barrier(device_ids=[self.local])
+            else:
+                self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.dist is None:
+            return x
+        import torch
+        dev = f"cuda:{self.local}" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            import torch
+            ident = "GPU-" + str(torch.cuda.get_device_properties(self.idx).uuid)
+        except Exception:
+            ident = str(self.idx)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-i", ident, "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- helpers
+def peak_hbm() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def cores_used() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def algo_code(name):
+    import ring_all_reduce_ddp_gb300 as D
+    return {"fused": D.DDP_ALGO_FUSED, "ldst": D.DDP_ALGO_FUSED_LDST, "ring_steps": D.DDP_ALGO_RING_STEPS}[name]
+
+
+def kernel_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("k_reduce.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "ring_all_reduce_ddp_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sync_sample(cfg, budget_s: float, max_buckets=None):
+    """Time the oracle's gradient sync (flatten, literal ring all-reduce,
+    unflatten) bucket by bucket until the budget is used. Returns
+    (algorithmic bytes, seconds, description). Inputs are generated untimed."""
+    import numpy as np
+
+    from oracle import buckets as ob
+    from oracle import ring as orc
+    from synth import workloads as W
+    numel = W.numels(cfg)
+    starts = W.tensor_starts(cfg)
+    es = W.esize(cfg)
+    p = cfg["p"]
+    plan = ob.assign_buckets(numel, es, cfg["first_cap"], cfg["cap"])
+    _, offset, bnumel = ob.bucket_layout(numel, plan)
+    Dv = W.divisor(cfg)
+    total_bytes, total_t, done = 0, 0.0, []
+    for b, members in enumerate(plan):
+        if max_buckets is not None and len(done) >= max_buckets:
+            break
+        grads = [{t: W.host_values(cfg, r, np.arange(starts[t], starts[t] + numel[t])) for t in members}
+                 for r in range(p)]
+        t0 = time.perf_counter()
+        flats = []
+        for r in range(p):
+            flats.append(ob.flatten([grads[r].get(t, np.zeros(0, np.float32 if es == 4 else np.uint16))
+                                     for t in range(len(numel))], members, offset, bnumel[b]))
+        outs, _ = orc.allreduce(flats, bnumel[b], Dv, cfg["dtype"])
+        for r in range(p):
+            ob.unflatten(outs[r], members, offset, numel)
+        total_t += time.perf_counter() - t0
+        total_bytes += 3 * 2 * p * bnumel[b] * es
+        done.append(b)
+        if total_t >= budget_s:
+            break
+    desc = (f"oracle flatten + literal ring all-reduce + unflatten of buckets {done} "
+            f"({sum(bnumel[b] for b in done)} of {sum(bnumel)} elements per replica, p={p}), single thread")
+    return total_bytes, total_t, desc
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, ranks: Ranks):
+    import torch
+
+    import ring_all_reduce_ddp_gb300 as D
+    from ring_all_reduce_ddp_gb300 import build as B
+    from ring_all_reduce_ddp_gb300.reducer import Reducer, broadcast_buffers
+    from synth import workloads as W
+
+    B.build_library()
+    dev = ranks.local if torch.cuda.device_count() > 1 else 0
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.config]
+    p = cfg["p"]
+    algo = algo_code(args.algo)
+    grads, arenas = W.make_grads(cfg, f"cuda:{dev}")
+    bufs = W.buffer_set(cfg, f"cuda:{dev}") if cfg.get("buffers") else None
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    divisor = W.divisor(cfg)
+    stream = torch.cuda.current_stream()
+    bc_algo = D.DDP_ALGO_RING_STEPS if args.algo == "ring_steps" else D.DDP_ALGO_FUSED
+    buf_bytes = sum(t.numel() * t.element_size() for t in bufs[0]) if bufs else 0
+
+    def step(events=None):
+        if not red.assign():
+            raise RuntimeError("bucket assignment changed")
+        if bufs:
+            broadcast_buffers(bufs, 0, 0, bc_algo, stream)
+        red.sync_gradients(divisor, algo, stream=stream, allreduce_events=events)
+
+    ab = red.algorithmic_bytes()
+    step_bytes = ab["total"] + p * buf_bytes
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    ranks.barrier()
+
+    sampler = ClockSampler(dev)
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = D.ddp_kernel_launches()
+    ar_events: list = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(ar_events)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    launches = D.ddp_kernel_launches() - launches0
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    ms_max = ranks.max(ms)
+    ms_per_step = ms_max / args.steps
+    value = step_bytes * args.steps * ranks.world / (ms_max / 1e3) / 1e9
+
+    # dominant kernel: the fused all-reduce, timed per launch with events on its stream
+    ar_ms = [a.elapsed_time(b) for a, b in ar_events]
+    ar_bytes_per_launch = [2 * p * n * W.esize(cfg) for n in red.bucket_numel] * args.steps
+    achieved = sum(ar_bytes_per_launch) / (sum(ar_ms) / 1e3) / 1e9
+    peak, peak_kind = peak_hbm()
+    traffic = None
+    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]:
+        traffic = int(NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * (ab["allreduce"] / len(red.buckets)))
+    bucket_mb = [round(n * W.esize(cfg) / 2 ** 20, 2) for n in red.bucket_numel]
+
+    # end to end through the public API: pinned host gradients in, synchronised gradients out
+    if True:
+        host_in = [a.detach().to("cpu").pin_memory() for a in arenas]
+        host_out = [torch.empty_like(h).pin_memory() for h in host_in]
+        k_e2e = args.steps
+        for _ in range(min(3, max(args.warmup, 1))):
+            for a, h in zip(arenas, host_in):
+                a.copy_(h, non_blocking=True)
+            step()
+            for a, h in zip(arenas, host_out):
+                h.copy_(a, non_blocking=True)
+        torch.cuda.synchronize()
+        ranks.barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(k_e2e):
+            for a, h in zip(arenas, host_in):
+                a.copy_(h, non_blocking=True)
+            step()
+            for a, h in zip(arenas, host_out):
+                h.copy_(a, non_blocking=True)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        ranks.barrier()
+        e2e_ms = ranks.max(f0.elapsed_time(f1))
+        io = sum(a.numel() * a.element_size() for a in arenas)
+        e2e = {"value": round(step_bytes * k_e2e * ranks.world / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "ms_per_step": round(e2e_ms / k_e2e, 4)}
+
+    cpu = None
+    if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
+        nb, secs, desc = oracle_sync_sample(cfg, args.cpu_budget_s)
+        cpu = {"value": round(nb / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
+               "host_cores_available": cores_used()}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ranks.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg["dtype"], "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "p": p, "buckets": len(red.buckets),
+                   "bucket_mb": bucket_mb, "algo": args.algo, "divisor": divisor,
+                   "l2": "inputs larger than L2: %.2f GB of gradients + %.2f GB of buckets per step" %
+                         (sum(a.numel() * a.element_size() for a in arenas) / 1e9, ab["allreduce"] / 2 / 1e9),
+                   "parallelism": f"replicas only: {ranks.world} independent GPU(s)"},
+        "roofline": {"bound": "hbm", "kernel": "fused ring-order all-reduce", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": int(ab["allreduce"] / len(red.buckets)),
+                     "avg_launch_us": round(1e3 * statistics.mean(ar_ms), 2)},
+        "allreduce_gbs": round(achieved, 1),
+        "buckets_per_s": round(len(red.buckets) * args.steps * ranks.world / (ms_max / 1e3), 1),
+        "busbw_gbs": round(sum(n * W.esize(cfg) for n in red.bucket_numel) / (sum(ar_ms) / args.steps / 1e3)
+                           / 1e9 * 2 * (p - 1) / p, 1),
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+    }
+    if ranks.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- reference arm
+def run_reference(args, ranks: Ranks):
+    """The CPU oracle as it stands, on rank 0 only: each step is the oracle's
+    sync of the workload's first bucket (a bounded sample)."""
+    if ranks.rank != 0:
+        return
+    from synth import workloads as W
+    cfg = W.CONFIGS[args.config]
+    for _ in range(max(args.warmup, 0)):
+        oracle_sync_sample(cfg, 0.0, max_buckets=1)
+    nb_tot, t_tot, desc = 0, 0.0, ""
+    for _ in range(args.steps):
+        nb, t, desc = oracle_sync_sample(cfg, 0.0, max_buckets=1)
+        nb_tot += nb
+        t_tot += t
+    value = nb_tot / t_tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ranks.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_tot / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": W.CONFIGS[args.config]["dtype"],
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "p": cfg["p"], "algo": "oracle literal ring"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle", "cores": 1, "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- sweep
+def run_sweep(args, ranks: Ranks):
+    """Message-size / rank-count sweep: one fp32 buffer of M = 1 KiB * 4^k bytes
+    on each of p replicas (p * M <= 64 GiB), values uniform on [-1, 1);
+    all-reduce, reduce-scatter (both ownerships), all-gather and broadcast in
+    the fused and the literal form. One JSON line per point: median of the
+    per-launch CUDA-event times, L2 flushed (a 512 MiB write) before each
+    launch whose working set is under 2x L2."""
+    import torch
+
+    import ring_all_reduce_ddp_gb300 as D
+    from ring_all_reduce_ddp_gb300 import build as B
+    import synth
+    B.build_library()
+    if ranks.rank != 0:
+        return
+    torch.cuda.set_device(0)
+    peak, peak_kind = peak_hbm()
+    ps = [int(x) for x in os.environ.get("SWEEP_P", "2,4,8,16,64").split(",")]
+    max_k = int(os.environ.get("SWEEP_MAX_K", "10"))
+    ops = os.environ.get("SWEEP_OPS", "allreduce,reduce_scatter_rank,reduce_scatter_ring,allgather,broadcast")
+    algos = os.environ.get("SWEEP_ALGOS", "fused,ring_steps").split(",")
+    reps = int(os.environ.get("SWEEP_REPS", "20"))
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    for p in ps:
+        for k in range(max_k + 1):
+            M = 1024 * 4 ** k
+            if p * M > 64 << 30:
+                continue
+            n = M // 4
+            bufs = []
+            for r in range(p):
+                t = torch.empty(n, dtype=torch.float32, device="cuda")
+                synth.fill_(t, "uniform", 1005, r)
+                bufs.append(t)
+            m = n // p
+            outs = [torch.empty(max(n, p * m), dtype=torch.float32, device="cuda") for _ in range(p)] \
+                if ops != "allreduce" else []
+            for op in ops.split(","):
+                for an in algos:
+                    al = algo_code(an)
+                    if op == "allreduce":
+                        fn = lambda: D.ddp_allreduce(bufs, n, D.DDP_FLOAT32, float(p), al)
+                        nbytes = 2 * p * M
+                    elif op.startswith("reduce_scatter"):
+                        own = D.DDP_OWN_RANK if op.endswith("rank") else D.DDP_OWN_RING
+                        fn = lambda: D.ddp_reduce_scatter(bufs, outs, n, D.DDP_FLOAT32, 1.0, own, al)
+                        nbytes = p * M + M
+                    elif op == "allgather":
+                        fn = lambda: D.ddp_allgather(bufs, outs, m, D.DDP_FLOAT32, D.DDP_OWN_RANK, al)
+                        nbytes = M + p * M
+                    else:
+                        fn = lambda: D.ddp_broadcast(bufs, M, 0, al)
+                        nbytes = p * M
+                    small = nbytes < 2 * l2
+                    for _ in range(3):
+                        fn()
+                    times = []
+                    for _ in range(reps):
+                        if small:
+                            flush.fill_(1)
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record()
+                        fn()
+                        b.record()
+                        b.synchronize()
+                        times.append(a.elapsed_time(b))
+                    t = statistics.median(times) / 1e3
+                    gbs = nbytes / t / 1e9
+                    line = {"sweep": op, "algo": an, "p": p, "bytes": M, "us": round(t * 1e6, 2),
+                            "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                            "busbw_gbs": round(M / t / 1e9 * 2 * (p - 1) / p, 1) if op == "allreduce" else None,
+                            "l2_flushed": small}
+                    print(json.dumps(line), flush=True)
+            del bufs, outs
+            torch.cuda.empty_cache()
+
+
+def main():
+    args = parse_args()
+    ranks = Ranks()
+    try:
+        if args.sweep:
+            run_sweep(args, ranks)
+        elif args.impl == "reference":
+            run_reference(args, ranks)
+        else:
+            run_ours(args, ranks)
+    finally:
+        ranks.close()
+
+
+if __name__ == "__main__":
+    main()

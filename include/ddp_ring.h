@@ -1,0 +1,260 @@
+/*
+ * ddp_ring.h -- C ABI of a single-GPU library for the hot path of PyTorch
+ * DDP's Reducer: bucketed gradient all-reduce by the two-pass ring, with p
+ * simulated ranks whose replica buffers all live in one GPU's memory.
+ *
+ * Sources, by page title and section:
+ *   [DDP]  "PyTorch DDP Deep Dive -- Initialization, Buffer Broadcast, the
+ *          Reducer, and the torch.compile Story"
+ *   [COLL] "Collective Ops From Scratch"
+ *   [DP]   "Data parallelism"
+ *
+ * Conventions (every call):
+ *   - Pointer arrays (bufs, in, out, grads, tensors, bucket) are HOST arrays of
+ *     DEVICE pointers. They are read during the call and not kept, except by a
+ *     ddp_ring handle, which keeps a copy until ddp_ring_destroy.
+ *   - The caller owns every replica, input and output buffer. The library
+ *     allocates only: a handle's workspace (freed by ddp_ring_destroy), and,
+ *     for the literal ring schedule of a few one-shot calls, a stream-ordered
+ *     temporary (cudaMallocAsync / cudaFreeAsync on the caller's stream).
+ *   - Work is enqueued on the caller's stream and runs asynchronously to the
+ *     host, as DDP's per-bucket futures do ([DDP] Part 2, "Step 3:
+ *     finalize_backward"). No call synchronizes the device except
+ *     ddp_ring_sync and ddp_device_error.
+ *   - Errors: every call returns a ddp_status. Argument errors are found on the
+ *     host before anything is enqueued. A failed launch returns
+ *     DDP_ERR_CUDA. ddp_last_error() gives this thread's last message.
+ *   - Replica buffers of one call must be distinct and must not overlap.
+ *     Alignment is not required; misaligned heads and tails take a scalar path.
+ *   - 1 <= p <= DDP_MAX_P. n == 0 (or nbytes == 0) is a no-op returning DDP_OK.
+ *   - Floating point: the sum of p contributions is accumulated in fp32 in
+ *     ring order, by IEEE round-to-nearest additions (no FMA contraction, no
+ *     reassociation); the scale is one IEEE division; bf16 results are
+ *     rounded to nearest even once, at the end.
+ */
+#ifndef DDP_RING_H
+#define DDP_RING_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DDP_MAX_P 256
+
+typedef enum {
+  DDP_OK = 0,
+  DDP_ERR_ARG = 1,            /* bad argument (null pointer, range, aliasing)      */
+  DDP_ERR_DTYPE = 2,          /* unsupported or mismatched element type            */
+  DDP_ERR_NOT_DIVISIBLE = 3,  /* torch-contract reduce_scatter with p not dividing n */
+  DDP_ERR_ALIGN = 4,          /* reserved                                          */
+  DDP_ERR_NOMEM = 5,          /* a device allocation failed                        */
+  DDP_ERR_CUDA = 6,           /* a CUDA call or launch failed                      */
+  DDP_ERR_TIMEOUT = 7,        /* a bounded device-side wait gave up                */
+  DDP_ERR_STATE = 8           /* handle used out of order (e.g. step after the last) */
+} ddp_status;
+
+typedef enum { DDP_FLOAT32 = 0, DDP_BFLOAT16 = 1 } ddp_dtype;
+
+typedef enum {
+  DDP_ALGO_FUSED = 0,       /* one pass: read p contributions, write p results    */
+  DDP_ALGO_RING_STEPS = 1,  /* the literal schedule: one launch per ring step      */
+  DDP_ALGO_FUSED_LDST = 2   /* one pass, register-only variant (no shared memory)  */
+} ddp_algo;
+
+typedef enum {
+  DDP_OWN_RANK = 0,  /* rank r <-> chunk r: the torch contract, chunks pre-rotated */
+  DDP_OWN_RING = 1   /* rank r <-> chunk (r+1) mod p: where pass 1 leaves them     */
+} ddp_own;
+
+typedef enum {
+  DDP_ORDER_REVERSED = 0,     /* walk last-registered first; bucket 0 gets the first cap   */
+  DDP_ORDER_REGISTRATION = 1  /* walk in registration order, first cap on that walk's
+                                 bucket 0, then reverse the bucket list                  */
+} ddp_border;
+
+typedef enum {
+  DDP_OP_ALLREDUCE = 0,
+  DDP_OP_REDUCE_SCATTER = 1,
+  DDP_OP_ALLGATHER = 2,
+  DDP_OP_BROADCAST = 3
+} ddp_op;
+
+/* ------------------------------------------------------------------ buckets */
+
+/* Bucket assignment by size. [DDP] Part 1, "What _ddp_init_helper actually
+ * does" (buckets handed to the Reducer reversed; small first bucket, 1 MB by
+ * default) and Part 3, DDPOptimizer's compile_fn (reverse walk; a new bucket
+ * once the current one reaches bucket_bytes_cap, or first_bucket_cap for the
+ * first); [DP] "Overlapping communication with the backward pass" (~25 MB).
+ *
+ * Walks the k tensors in `order`; each whole tensor joins the open bucket; the
+ * bucket closes once its byte size (elements * elem_size) is >= its cap:
+ * first_bucket_cap_bytes for bucket 0, bucket_cap_bytes after. Tensors are
+ * never split; no empty bucket is produced. Host-only: no CUDA call.
+ *   numel[k]            element count of tensor t, registration order, >= 0
+ *   out n_buckets       number of buckets B (0 when k == 0)
+ *   out bucket_of[k]    bucket of tensor t
+ *   out offset[k]       element offset of tensor t inside its bucket
+ *                       (exclusive prefix sum in walk order)
+ *   out bucket_ptr[k+1] CSR row pointers: bucket b's tensors are
+ *                       bucket_tensors[bucket_ptr[b] .. bucket_ptr[b+1])
+ *   out bucket_tensors[k] tensor indices in walk order
+ *   out bucket_numel[k] element count of each bucket (first B entries used)
+ * Errors: DDP_ERR_ARG for k < 0, null arrays (k > 0), elem_size <= 0,
+ * negative numel or caps, or an unknown order. */
+ddp_status ddp_bucket_assign(int32_t k, const int64_t* numel, int32_t elem_size,
+                             int64_t first_bucket_cap_bytes, int64_t bucket_cap_bytes,
+                             ddp_border order, int32_t* n_buckets, int32_t* bucket_of,
+                             int64_t* offset, int32_t* bucket_ptr, int32_t* bucket_tensors,
+                             int64_t* bucket_numel);
+
+/* Copy each replica's k gradients into its flat bucket. [DDP] Part 2
+ * "Step 2: backward", mark_variable_ready: each parameter's gradient is
+ * copied into its slice of the bucket's flat tensor, optionally pre-divided.
+ *   grads[p*k]  grads[r*k + j]: replica r's tensor j (numel[j] elements, dtype)
+ *   numel[k], offset[k]: element count and bucket offset of tensor j
+ *   bucket[p]   replica r's flat bucket (>= max(offset[j]+numel[j]) elements)
+ *   predivide   1.0f: plain copy; otherwise y = round(fl32(x / predivide))
+ * Tensors must not overlap the buckets. Zero-element tensors are skipped. */
+ddp_status ddp_bucket_flatten(int32_t p, int32_t k, const void* const* grads,
+                              const int64_t* numel, const int64_t* offset,
+                              void* const* bucket, ddp_dtype dtype, float predivide,
+                              cudaStream_t stream);
+
+/* Copy each replica's flat bucket back into its k gradients (the inverse of
+ * ddp_bucket_flatten). [DDP] Part 2 "Step 3: finalize_backward": the reduced
+ * flat tensor is copied back into the per-parameter gradient views (skipped by
+ * callers whose gradients are already bucket views). Same layout as above. */
+ddp_status ddp_bucket_unflatten(int32_t p, int32_t k, const void* const* bucket,
+                                const int64_t* numel, const int64_t* offset,
+                                void* const* grads, ddp_dtype dtype, cudaStream_t stream);
+
+/* ------------------------------------------------------------ collectives */
+
+/* All-reduce in place over p replica buffers of n elements. [COLL] "Ring
+ * allreduce in two passes"; [DP] "Ring all-reduce, derived" and "Overlapping
+ * communication with the backward pass" (DDP divides the sum by the number of
+ * ranks); [DP] "Why averaging gradients is exactly large-batch training"
+ * (divide once by the global token count).
+ * With cs = ceil(n/p) and chunk c = [c*cs, min(n, (c+1)*cs)), every element i
+ * of chunk c becomes, on every replica,
+ *     y = fl32( (((x_c + x_{c+1}) + x_{c+2}) + ... + x_{c+p-1}) / divisor )
+ * with replica indices mod p: the order in which the ring's reduce-scatter
+ * accumulates chunk c, starting at rank c. bf16 inputs are widened to fp32,
+ * and y is rounded to bf16 (nearest even). divisor: 1 (sum), p (average) or a
+ * token count; must be finite and non-zero.
+ * algo DDP_ALGO_FUSED / DDP_ALGO_FUSED_LDST: one pass; RING_STEPS: 2(p-1)
+ * launches of the literal schedule (bf16 keeps fp32 partials in a temporary). */
+ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype,
+                         float divisor, ddp_algo algo, cudaStream_t stream);
+
+/* Reduce-scatter: pass 1 alone. [COLL] code/main.py list (reduce_scatter
+ * pre-rotates so rank r returns the sum of chunk r and rejects element counts
+ * not divisible by the world size); [DP] "The collective operations".
+ *   in[p]:  n elements each (not modified)
+ *   out[p]: DDP_OWN_RANK: out[r] = chunk r, summed from rank r+1 around to
+ *           rank r; needs p | n (else DDP_ERR_NOT_DIVISIBLE), n/p elements.
+ *           DDP_OWN_RING: out[q] = chunk (q+1) mod p, summed from rank q+1;
+ *           only the chunk's real elements are written (the padding is
+ *           trimmed); out[q] needs room for ceil(n/p) elements.
+ * Each value is fl32(sum / divisor), rounded to dtype. out must not overlap in. */
+ddp_status ddp_reduce_scatter(const void* const* in, void* const* out, int32_t p, int64_t n,
+                              ddp_dtype dtype, float divisor, ddp_own own, ddp_algo algo,
+                              cudaStream_t stream);
+
+/* All-gather: pass 2 alone. [COLL] code/main.py list (N-1 rotations);
+ * [DP] "Ring all-reduce, derived" (all-gather step k sends chunk (r+1-k) mod p).
+ *   in[p]:  m elements each: rank r's finished chunk, chunk r (DDP_OWN_RANK) or
+ *           chunk (r+1) mod p (DDP_OWN_RING)
+ *   out[p]: p*m elements each; every out[r] ends holding all chunks in order.
+ * A copy: bit-exact, no scaling. out must not overlap in. */
+ddp_status ddp_allgather(const void* const* in, void* const* out, int32_t p, int64_t m,
+                         ddp_dtype dtype, ddp_own own, ddp_algo algo, cudaStream_t stream);
+
+/* Broadcast nbytes from bufs[root] to every other replica. [COLL] code/main.py
+ * list (broadcast over a doubling tree). RING_STEPS runs the tree: with
+ * v = (r - root) mod p, at step j every v < 2^j copies to v + 2^j (< p);
+ * ceil(log2 p) launches. FUSED reads the root once and writes p-1 copies. */
+ddp_status ddp_broadcast(void* const* bufs, int32_t p, int64_t nbytes, int32_t root,
+                         ddp_algo algo, cudaStream_t stream);
+
+/* Coalesced broadcast of k tensors from replica root. [DDP] Part 2, the
+ * annotated trace: dist._broadcast_coalesced packs tensors into buckets of at
+ * most 250 * 1024 * 1024 bytes, flattens each, broadcasts it from the root,
+ * unflattens and copies back; this is the per-forward buffer sync of DDP
+ * (BatchNorm running statistics).
+ *   tensors[p*k]: tensors[r*k + j] is replica r's tensor j, nbytes[j] bytes
+ *   bucket_cap_bytes: 0 means 250 MiB. Tensors join a bucket in order; a new
+ *   bucket starts when the next tensor would take it over the cap.
+ * RING_STEPS packs each bucket on the root, runs the doubling tree on the
+ * packed buffers (a temporary of p * bucket bytes) and unpacks; FUSED copies
+ * each root tensor straight to the p-1 others (same bytes). */
+ddp_status ddp_broadcast_coalesced(int32_t p, int32_t k, void* const* tensors,
+                                   const int64_t* nbytes, int32_t root,
+                                   int64_t bucket_cap_bytes, ddp_algo algo,
+                                   cudaStream_t stream);
+
+/* ------------------------------------------- literal schedule, stepwise */
+
+/* A handle that runs one collective's literal schedule one step at a time, so
+ * the state after every step can be read. [COLL] "Ring allreduce in two
+ * passes"; [DP] "Ring all-reduce, derived".
+ *   op ALLREDUCE:      bufs = in (in place, n elements), out = NULL.
+ *                      2(p-1) steps (1 for p == 1): step s < p-1 is
+ *                      reduce-scatter step s (rank r's chunk (r-s) mod p is
+ *                      accumulated into rank r+1; the last one also divides the
+ *                      owner's chunk by divisor); then all-gather steps.
+ *                      fp32 partials live in the buffers; bf16 partials in the
+ *                      handle's fp32 workspace.
+ *   op REDUCE_SCATTER: in (n elements), out (as ddp_reduce_scatter); p-1 steps
+ *                      (1 for p == 1); partials in the workspace.
+ *   op ALLGATHER:      in (m = n elements), out (p*n); p-1 steps (1 for p == 1);
+ *                      step 0 also places each rank's own chunk.
+ *   op BROADCAST:      in = bufs (n bytes), out = NULL, root; ceil(log2 p) steps.
+ * Workspace (REDUCE_SCATTER, and bf16 ALLREDUCE): 2 * p * ceil(n/p) fp32,
+ * laid out [2][p][ceil(n/p)]; reduce-scatter step s writes half (s & 1), slot
+ * d = receiving rank, element e = offset inside the chunk.
+ * The handle keeps copies of the pointer arrays and enqueues on `stream`. */
+typedef struct ddp_ring ddp_ring;
+
+ddp_status ddp_ring_create(ddp_ring** handle, ddp_op op, void* const* in, void* const* out,
+                           int32_t p, int64_t n, ddp_dtype dtype, float divisor, ddp_own own,
+                           int32_t root, cudaStream_t stream);
+/* Total number of steps; -1 for a null handle. */
+int32_t ddp_ring_num_steps(const ddp_ring* handle);
+/* Steps enqueued so far; -1 for a null handle. */
+int32_t ddp_ring_steps_done(const ddp_ring* handle);
+/* Enqueue the next step. DDP_ERR_STATE once all steps are enqueued. */
+ddp_status ddp_ring_step(ddp_ring* handle);
+/* The fp32 workspace (NULL and 0 if this handle has none). */
+ddp_status ddp_ring_workspace(const ddp_ring* handle, void** fp32_partials,
+                              int64_t* elems_per_slot);
+/* Bytes rank `rank` has sent so far on the simulated wire: each ring send is
+ * one chunk of ceil(n/p) elements (padding included) at the buffer's element
+ * size; each tree send is n bytes. */
+ddp_status ddp_ring_bytes_sent(const ddp_ring* handle, int32_t rank, int64_t* bytes);
+/* Wait for the handle's stream and report any device-side error. */
+ddp_status ddp_ring_sync(ddp_ring* handle);
+/* Free the handle and its workspace (after the stream's work is done). */
+ddp_status ddp_ring_destroy(ddp_ring* handle);
+
+/* ----------------------------------------------------------------- misc */
+
+/* Synchronize `stream`, then read and clear the library's device error word:
+ * *code = 0 when no kernel reported a problem, else the first code a kernel
+ * recorded (a bounded wait that gave up). Returns DDP_ERR_TIMEOUT if set. */
+ddp_status ddp_device_error(cudaStream_t stream, int32_t* code);
+/* Number of kernels this library has launched in this process. */
+int64_t ddp_kernel_launches(void);
+/* Text of this thread's last error (empty if none). */
+const char* ddp_last_error(void);
+/* Fixed name of a status code. */
+const char* ddp_status_string(ddp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DDP_RING_H */

@@ -1,0 +1,793 @@
+// The C ABI (include/ddp_ring.h): argument checks, the host planner (bucket
+// assignment, chunk plan, coalescing groups, the literal schedule's steps) and
+// dispatch to the kernels. Everything that touches the data runs in the
+// library's kernels; this file only plans and launches.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "launch.h"
+
+using namespace ddp;
+
+namespace {
+
+thread_local std::string t_error;
+
+ddp_status fail(ddp_status s, const std::string& msg) {
+  t_error = msg;
+  return s;
+}
+
+ddp_status cuda_fail(cudaError_t e, const char* where) {
+  t_error = std::string(where) + ": " + cudaGetErrorString(e);
+  return DDP_ERR_CUDA;
+}
+
+#define DDP_CUDA(call, where)                         \
+  do {                                                \
+    cudaError_t e_ = (call);                          \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+  } while (0)
+
+#define DDP_CHECK(cond, code, msg) \
+  do {                             \
+    if (!(cond)) return fail(code, msg); \
+  } while (0)
+
+int esize(ddp_dtype dt) { return dt == DDP_FLOAT32 ? 4 : 2; }
+
+ddp_status check_common(int32_t p, int64_t n, int dtype) {
+  DDP_CHECK(p >= 1 && p <= DDP_MAX_P, DDP_ERR_ARG, "p must be in [1, " + std::to_string(DDP_MAX_P) + "]");
+  DDP_CHECK(n >= 0, DDP_ERR_ARG, "element count must be >= 0");
+  DDP_CHECK(dtype == DDP_FLOAT32 || dtype == DDP_BFLOAT16, DDP_ERR_DTYPE, "dtype must be DDP_FLOAT32 or DDP_BFLOAT16");
+  return DDP_OK;
+}
+
+ddp_status check_divisor(float d) {
+  DDP_CHECK(std::isfinite(d) && d != 0.0f, DDP_ERR_ARG, "divisor must be finite and non-zero");
+  return DDP_OK;
+}
+
+ddp_status check_ptrs(const void* const* v, int32_t count, const char* what) {
+  DDP_CHECK(v != nullptr, DDP_ERR_ARG, std::string(what) + " array is null");
+  for (int32_t i = 0; i < count; ++i)
+    DDP_CHECK(v[i] != nullptr, DDP_ERR_ARG, std::string(what) + "[" + std::to_string(i) + "] is null");
+  return DDP_OK;
+}
+
+// Byte ranges [begin, end) must be pairwise disjoint (empty ranges ignored).
+bool disjoint(std::vector<std::pair<uintptr_t, uintptr_t>> r) {
+  r.erase(std::remove_if(r.begin(), r.end(), [](const auto& x) { return x.second <= x.first; }), r.end());
+  std::sort(r.begin(), r.end());
+  for (size_t i = 1; i < r.size(); ++i)
+    if (r[i].first < r[i - 1].second) return false;
+  return true;
+}
+
+std::pair<uintptr_t, uintptr_t> range_of(const void* ptr, int64_t bytes) {
+  const uintptr_t b = reinterpret_cast<uintptr_t>(ptr);
+  return {b, b + static_cast<uintptr_t>(bytes)};
+}
+
+int64_t chunk_size(int64_t n, int32_t p) { return n > 0 ? (n + p - 1) / p : 0; }
+
+bool same_align16(const void* const* v, int32_t count) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(v[0]) & 15u;
+  for (int32_t i = 1; i < count; ++i)
+    if ((reinterpret_cast<uintptr_t>(v[i]) & 15u) != a0) return false;
+  return true;
+}
+
+// ------------------------------------------------------------------ planner
+
+// Fused one-pass reduction of p replicas.
+ddp_status run_fused(const void* const* in, void* const* out, int32_t p, int64_t n, ddp_dtype dt,
+                     float divisor, bool scatter, int shift, bool staged, cudaStream_t s) {
+  FusedArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int j = 0; j < 2 * p; ++j) a.src[j] = in[j % p];
+  for (int r = 0; r < p; ++r) a.dst[r] = out[r];
+  a.n = n;
+  a.cs = chunk_size(n, p);
+  a.divisor = divisor;
+  a.p = p;
+  a.scatter = scatter ? 1 : 0;
+  a.shift = shift;
+  // All-reduce reads and writes the same p replicas; a scatter's outputs are
+  // checked per chunk in the kernel.
+  a.same_align = same_align16(in, p) ? 1 : 0;
+  DDP_CUDA(launch_fused_reduce(a, dt, staged, s), "fused reduction launch");
+  return DDP_OK;
+}
+
+// The literal schedule of one collective, one step at a time.
+struct Plan {
+  ddp_op op = DDP_OP_ALLREDUCE;
+  int32_t p = 1;
+  int64_t n = 0;  // AR/RS: elements per input; AG: elements per input (m); BC: bytes
+  ddp_dtype dt = DDP_FLOAT32;
+  float divisor = 1.0f;
+  ddp_own own = DDP_OWN_RANK;
+  int32_t root = 0;
+  std::vector<void*> in, out;
+  int64_t cs = 0;
+  float* ws = nullptr;
+  bool ws_async = false;
+  int32_t nsteps = 0, done = 0;
+  std::vector<int64_t> sent;
+
+  bool needs_ws() const {
+    return p > 1 && ((op == DDP_OP_ALLREDUCE && dt == DDP_BFLOAT16) || op == DDP_OP_REDUCE_SCATTER);
+  }
+  int64_t ws_elems() const { return 2 * static_cast<int64_t>(p) * cs; }
+
+  void init() {
+    cs = (op == DDP_OP_ALLGATHER) ? n : chunk_size(n, p);
+    switch (op) {
+      case DDP_OP_ALLREDUCE: nsteps = p == 1 ? 1 : 2 * (p - 1); break;
+      case DDP_OP_REDUCE_SCATTER:
+      case DDP_OP_ALLGATHER: nsteps = p == 1 ? 1 : p - 1; break;
+      case DDP_OP_BROADCAST: {
+        int steps = 0;
+        for (int64_t span = 1; span < p; span *= 2) ++steps;
+        nsteps = steps;
+        break;
+      }
+    }
+    sent.assign(p, 0);
+  }
+
+  ddp_status step(cudaStream_t s) {
+    if (done >= nsteps) return fail(DDP_ERR_STATE, "all steps of this schedule are already enqueued");
+    const int st = done;
+    const int es = (op == DDP_OP_BROADCAST) ? 1 : esize(dt);
+    ddp_status rc = DDP_OK;
+    if (op == DDP_OP_ALLREDUCE) {
+      if (p == 1) {
+        rc = run_fused(in.data(), in.data(), 1, n, dt, divisor, false, 0, false, s);
+      } else if (st < p - 1) {
+        RingStepArgs a;
+        std::memset(&a, 0, sizeof(a));
+        for (int r = 0; r < p; ++r) { a.x[r] = in[r]; a.out[r] = in[r]; }
+        a.w = ws; a.n = n; a.cs = cs; a.divisor = divisor; a.p = p; a.step = st;
+        a.shift = 0; a.last = (st == p - 2); a.out_rel = 0;
+        DDP_CUDA(dt == DDP_FLOAT32 ? launch_rs_step_inplace_f32(a, s) : launch_rs_step_ws(a, dt, s),
+                 "reduce-scatter step launch");
+        for (int r = 0; r < p; ++r) sent[r] += cs * es;
+      } else {
+        const int k = st - (p - 1);
+        PairCopyArgs a;
+        std::memset(&a, 0, sizeof(a));
+        for (int r = 0; r < p; ++r) {
+          const int c = ((r + 1 - k) % p + p) % p;
+          const int64_t lo = std::min(n, c * cs), hi = std::min(n, (c + 1) * cs);
+          a.src[r] = static_cast<const char*>(in[r]) + lo * es;
+          a.dst[r] = static_cast<char*>(in[(r + 1) % p]) + lo * es;
+          a.nbytes[r] = (hi - lo) * es;
+          sent[r] += cs * es;
+        }
+        a.njobs = p;
+        DDP_CUDA(launch_pair_copy(a, s), "all-gather step launch");
+      }
+    } else if (op == DDP_OP_REDUCE_SCATTER) {
+      if (p == 1) {
+        rc = run_fused(in.data(), out.data(), 1, n, dt, divisor, true, 0, false, s);
+      } else {
+        RingStepArgs a;
+        std::memset(&a, 0, sizeof(a));
+        for (int r = 0; r < p; ++r) { a.x[r] = in[r]; a.out[r] = out[r]; }
+        a.w = ws; a.n = n; a.cs = cs; a.divisor = divisor; a.p = p; a.step = st;
+        a.shift = (own == DDP_OWN_RANK) ? 1 : 0; a.last = (st == p - 2); a.out_rel = 1;
+        DDP_CUDA(launch_rs_step_ws(a, dt, s), "reduce-scatter step launch");
+        for (int r = 0; r < p; ++r) sent[r] += cs * es;
+      }
+    } else if (op == DDP_OP_ALLGATHER) {
+      const int64_t mb = n * es;
+      if (p == 1) {
+        PairCopyArgs a;
+        std::memset(&a, 0, sizeof(a));
+        a.src[0] = static_cast<const char*>(in[0]); a.dst[0] = static_cast<char*>(out[0]);
+        a.nbytes[0] = mb; a.njobs = 1;
+        DDP_CUDA(launch_pair_copy(a, s), "all-gather copy launch");
+      } else {
+        auto held = [&](int r) { return own == DDP_OWN_RANK ? r : (r + 1) % p; };
+        if (st == 0) {  // each rank's own chunk goes to its place in its output
+          PairCopyArgs a;
+          std::memset(&a, 0, sizeof(a));
+          for (int r = 0; r < p; ++r) {
+            a.src[r] = static_cast<const char*>(in[r]);
+            a.dst[r] = static_cast<char*>(out[r]) + held(r) * mb;
+            a.nbytes[r] = mb;
+          }
+          a.njobs = p;
+          DDP_CUDA(launch_pair_copy(a, s), "all-gather placement launch");
+        }
+        PairCopyArgs a;
+        std::memset(&a, 0, sizeof(a));
+        for (int r = 0; r < p; ++r) {
+          const int c = ((held(r) - st) % p + p) % p;
+          a.src[r] = (st == 0) ? static_cast<const char*>(in[r]) : static_cast<const char*>(out[r]) + c * mb;
+          a.dst[r] = static_cast<char*>(out[(r + 1) % p]) + c * mb;
+          a.nbytes[r] = mb;
+          sent[r] += mb;
+        }
+        a.njobs = p;
+        DDP_CUDA(launch_pair_copy(a, s), "all-gather step launch");
+      }
+    } else {  // broadcast: doubling tree
+      const int64_t span = int64_t(1) << st;
+      PairCopyArgs a;
+      std::memset(&a, 0, sizeof(a));
+      int jobs = 0;
+      for (int64_t v = 0; v < span; ++v) {
+        if (v + span >= p) continue;
+        const int src = static_cast<int>((root + v) % p), dst = static_cast<int>((root + v + span) % p);
+        a.src[jobs] = static_cast<const char*>(in[src]);
+        a.dst[jobs] = static_cast<char*>(in[dst]);
+        a.nbytes[jobs] = n;
+        sent[src] += n;
+        ++jobs;
+      }
+      a.njobs = jobs;
+      DDP_CUDA(launch_pair_copy(a, s), "broadcast step launch");
+    }
+    if (rc != DDP_OK) return rc;
+    ++done;
+    return DDP_OK;
+  }
+
+  ddp_status run_all(cudaStream_t s) {
+    while (done < nsteps) {
+      const ddp_status rc = step(s);
+      if (rc != DDP_OK) return rc;
+    }
+    return DDP_OK;
+  }
+};
+
+// One-shot literal schedule with a stream-ordered temporary workspace.
+ddp_status run_plan_once(Plan& pl, cudaStream_t s) {
+  pl.init();
+  if (pl.needs_ws()) {
+    void* w = nullptr;
+    DDP_CUDA(cudaMallocAsync(&w, pl.ws_elems() * sizeof(float), s), "workspace allocation");
+    pl.ws = static_cast<float*>(w);
+  }
+  const ddp_status rc = pl.run_all(s);
+  if (pl.ws) {
+    const cudaError_t e = cudaFreeAsync(pl.ws, s);
+    pl.ws = nullptr;
+    if (rc == DDP_OK && e != cudaSuccess) return cuda_fail(e, "workspace release");
+  }
+  return rc;
+}
+
+ddp_status check_algo(int algo) {
+  DDP_CHECK(algo == DDP_ALGO_FUSED || algo == DDP_ALGO_RING_STEPS || algo == DDP_ALGO_FUSED_LDST,
+            DDP_ERR_ARG, "unknown algo");
+  return DDP_OK;
+}
+
+ddp_status check_own(int own) {
+  DDP_CHECK(own == DDP_OWN_RANK || own == DDP_OWN_RING, DDP_ERR_ARG, "unknown ownership");
+  return DDP_OK;
+}
+
+#define DDP_TRY(expr)                 \
+  do {                                \
+    const ddp_status rc_ = (expr);    \
+    if (rc_ != DDP_OK) return rc_;    \
+  } while (0)
+
+// Multi-tensor copies, split into launches of at most kSegCap segments.
+struct SegBatcher {
+  SegCopyArgs a;
+  ddp_dtype dt;
+  cudaStream_t s;
+  SegBatcher(ddp_dtype dt_, float predivide, cudaStream_t s_) : dt(dt_), s(s_) {
+    std::memset(&a, 0, sizeof(a));
+    a.elem_size = esize(dt_);
+    a.predivide = predivide;
+  }
+  ddp_status add(const void* src, void* dst, int64_t bytes) {
+    if (bytes <= 0) return DDP_OK;
+    const int64_t tiles = (bytes + kSegTileBytes - 1) / kSegTileBytes;
+    if (a.nseg == kSegCap || static_cast<int64_t>(a.tile0[a.nseg]) + tiles > 0x7FFFFFFF) DDP_TRY(flush());
+    DDP_CHECK(tiles <= 0x7FFFFFFF, DDP_ERR_ARG, "tensor too large");
+    a.src[a.nseg] = static_cast<const char*>(src);
+    a.dst[a.nseg] = static_cast<char*>(dst);
+    a.bytes[a.nseg] = bytes;
+    a.tile0[a.nseg + 1] = a.tile0[a.nseg] + static_cast<int32_t>(tiles);
+    ++a.nseg;
+    return DDP_OK;
+  }
+  ddp_status flush() {
+    if (a.nseg == 0) return DDP_OK;
+    DDP_CUDA(launch_seg_copy(a, dt, s), "segment copy launch");
+    const int elem = a.elem_size;
+    const float pd = a.predivide;
+    std::memset(&a, 0, sizeof(a));
+    a.elem_size = elem;
+    a.predivide = pd;
+    return DDP_OK;
+  }
+};
+
+ddp_status check_bucket_args(int32_t p, int32_t k, const int64_t* numel, const int64_t* offset, int dtype) {
+  DDP_TRY(check_common(p, 0, dtype));
+  DDP_CHECK(k >= 0, DDP_ERR_ARG, "k must be >= 0");
+  if (k > 0) DDP_CHECK(numel && offset, DDP_ERR_ARG, "numel / offset arrays are null");
+  for (int32_t j = 0; j < k; ++j)
+    DDP_CHECK(numel[j] >= 0 && offset[j] >= 0, DDP_ERR_ARG, "numel and offset must be >= 0");
+  return DDP_OK;
+}
+
+ddp_status check_bucket_layout(int32_t p, int32_t k, const void* const* grads, const int64_t* numel,
+                               const int64_t* offset, const void* const* bucket, int es) {
+  DDP_TRY(check_ptrs(bucket, p, "bucket"));
+  DDP_CHECK(grads != nullptr || k == 0, DDP_ERR_ARG, "grads array is null");
+  int64_t extent = 0;
+  std::vector<std::pair<uintptr_t, uintptr_t>> slots, ranges;
+  for (int32_t j = 0; j < k; ++j) {
+    extent = std::max(extent, offset[j] + numel[j]);
+    slots.push_back({static_cast<uintptr_t>(offset[j]), static_cast<uintptr_t>(offset[j] + numel[j])});
+  }
+  DDP_CHECK(disjoint(slots), DDP_ERR_ARG, "bucket slots of different tensors overlap");
+  for (int32_t r = 0; r < p; ++r) {
+    ranges.push_back(range_of(bucket[r], extent * es));
+    for (int32_t j = 0; j < k; ++j) {
+      if (numel[j] == 0) continue;
+      const void* g = grads[static_cast<int64_t>(r) * k + j];
+      DDP_CHECK(g != nullptr, DDP_ERR_ARG, "grads[" + std::to_string(r * k + j) + "] is null");
+      ranges.push_back(range_of(g, numel[j] * es));
+    }
+  }
+  DDP_CHECK(disjoint(ranges), DDP_ERR_ARG, "gradient tensors and buckets must not overlap");
+  return DDP_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+struct ddp_ring {
+  Plan plan;
+  cudaStream_t stream;
+};
+
+ddp_status ddp_bucket_assign(int32_t k, const int64_t* numel, int32_t elem_size,
+                             int64_t first_bucket_cap_bytes, int64_t bucket_cap_bytes,
+                             ddp_border order, int32_t* n_buckets, int32_t* bucket_of,
+                             int64_t* offset, int32_t* bucket_ptr, int32_t* bucket_tensors,
+                             int64_t* bucket_numel) {
+  DDP_CHECK(k >= 0, DDP_ERR_ARG, "k must be >= 0");
+  DDP_CHECK(n_buckets && bucket_ptr, DDP_ERR_ARG, "output arrays are null");
+  DDP_CHECK(k == 0 || (numel && bucket_of && offset && bucket_tensors && bucket_numel), DDP_ERR_ARG,
+            "input or output arrays are null");
+  DDP_CHECK(elem_size > 0, DDP_ERR_ARG, "elem_size must be > 0");
+  DDP_CHECK(first_bucket_cap_bytes >= 0 && bucket_cap_bytes >= 0, DDP_ERR_ARG, "caps must be >= 0");
+  DDP_CHECK(order == DDP_ORDER_REVERSED || order == DDP_ORDER_REGISTRATION, DDP_ERR_ARG, "unknown order");
+  for (int32_t t = 0; t < k; ++t) DDP_CHECK(numel[t] >= 0, DDP_ERR_ARG, "numel must be >= 0");
+
+  // Walk, closing a bucket once its bytes reach its cap.
+  std::vector<std::vector<int32_t>> buckets;
+  std::vector<int32_t> open;
+  int64_t bytes = 0;
+  for (int32_t w = 0; w < k; ++w) {
+    const int32_t t = (order == DDP_ORDER_REVERSED) ? k - 1 - w : w;
+    open.push_back(t);
+    bytes += numel[t] * elem_size;
+    const int64_t cap = buckets.empty() ? first_bucket_cap_bytes : bucket_cap_bytes;
+    if (bytes >= cap) {
+      buckets.push_back(open);
+      open.clear();
+      bytes = 0;
+    }
+  }
+  if (!open.empty()) buckets.push_back(open);
+  if (order == DDP_ORDER_REGISTRATION) std::reverse(buckets.begin(), buckets.end());
+
+  int32_t pos = 0;
+  bucket_ptr[0] = 0;
+  for (size_t b = 0; b < buckets.size(); ++b) {
+    int64_t off = 0;
+    for (int32_t t : buckets[b]) {
+      bucket_of[t] = static_cast<int32_t>(b);
+      offset[t] = off;
+      off += numel[t];
+      bucket_tensors[pos++] = t;
+    }
+    bucket_numel[b] = off;
+    bucket_ptr[b + 1] = pos;
+  }
+  *n_buckets = static_cast<int32_t>(buckets.size());
+  return DDP_OK;
+}
+
+ddp_status ddp_bucket_flatten(int32_t p, int32_t k, const void* const* grads, const int64_t* numel,
+                              const int64_t* offset, void* const* bucket, ddp_dtype dtype,
+                              float predivide, cudaStream_t stream) {
+  DDP_TRY(check_bucket_args(p, k, numel, offset, dtype));
+  DDP_TRY(check_divisor(predivide));
+  const int es = esize(dtype);
+  DDP_TRY(check_bucket_layout(p, k, grads, numel, offset, const_cast<const void* const*>(bucket), es));
+  SegBatcher sb(dtype, predivide, stream);
+  for (int32_t r = 0; r < p; ++r)
+    for (int32_t j = 0; j < k; ++j)
+      DDP_TRY(sb.add(grads[static_cast<int64_t>(r) * k + j], static_cast<char*>(bucket[r]) + offset[j] * es,
+                     numel[j] * es));
+  return sb.flush();
+}
+
+ddp_status ddp_bucket_unflatten(int32_t p, int32_t k, const void* const* bucket, const int64_t* numel,
+                                const int64_t* offset, void* const* grads, ddp_dtype dtype,
+                                cudaStream_t stream) {
+  DDP_TRY(check_bucket_args(p, k, numel, offset, dtype));
+  const int es = esize(dtype);
+  DDP_TRY(check_bucket_layout(p, k, const_cast<const void* const*>(grads), numel, offset, bucket, es));
+  SegBatcher sb(dtype, 1.0f, stream);
+  for (int32_t r = 0; r < p; ++r)
+    for (int32_t j = 0; j < k; ++j)
+      DDP_TRY(sb.add(static_cast<const char*>(bucket[r]) + offset[j] * es, grads[static_cast<int64_t>(r) * k + j],
+                     numel[j] * es));
+  return sb.flush();
+}
+
+ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
+                         ddp_algo algo, cudaStream_t stream) {
+  DDP_TRY(check_common(p, n, dtype));
+  DDP_TRY(check_divisor(divisor));
+  DDP_TRY(check_algo(algo));
+  DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
+  const int es = esize(dtype);
+  std::vector<std::pair<uintptr_t, uintptr_t>> rg;
+  for (int r = 0; r < p; ++r) rg.push_back(range_of(bufs[r], n * es));
+  DDP_CHECK(disjoint(rg), DDP_ERR_ARG, "replica buffers overlap");
+  if (n == 0) return DDP_OK;
+  if (algo == DDP_ALGO_RING_STEPS) {
+    Plan pl;
+    pl.op = DDP_OP_ALLREDUCE; pl.p = p; pl.n = n; pl.dt = dtype; pl.divisor = divisor;
+    pl.in.assign(bufs, bufs + p);
+    return run_plan_once(pl, stream);
+  }
+  return run_fused(const_cast<const void* const*>(bufs), bufs, p, n, dtype, divisor, false, 0,
+                   algo == DDP_ALGO_FUSED, stream);
+}
+
+ddp_status ddp_reduce_scatter(const void* const* in, void* const* out, int32_t p, int64_t n, ddp_dtype dtype,
+                              float divisor, ddp_own own, ddp_algo algo, cudaStream_t stream) {
+  DDP_TRY(check_common(p, n, dtype));
+  DDP_TRY(check_divisor(divisor));
+  DDP_TRY(check_algo(algo));
+  DDP_TRY(check_own(own));
+  DDP_TRY(check_ptrs(in, p, "in"));
+  DDP_TRY(check_ptrs(const_cast<const void* const*>(out), p, "out"));
+  if (own == DDP_OWN_RANK)
+    DDP_CHECK(n % p == 0, DDP_ERR_NOT_DIVISIBLE,
+              "reduce_scatter: " + std::to_string(n) + " elements are not divisible by " + std::to_string(p) + " ranks");
+  const int es = esize(dtype);
+  const int64_t cs = chunk_size(n, p);
+  std::vector<std::pair<uintptr_t, uintptr_t>> outs, all;
+  for (int r = 0; r < p; ++r) outs.push_back(range_of(out[r], cs * es));
+  DDP_CHECK(disjoint(outs), DDP_ERR_ARG, "output buffers overlap");
+  for (int r = 0; r < p; ++r) {
+    all = outs;
+    all.push_back(range_of(in[r], n * es));
+    DDP_CHECK(disjoint(all), DDP_ERR_ARG, "an output buffer overlaps an input");
+  }
+  if (n == 0) return DDP_OK;
+  if (algo == DDP_ALGO_RING_STEPS) {
+    Plan pl;
+    pl.op = DDP_OP_REDUCE_SCATTER; pl.p = p; pl.n = n; pl.dt = dtype; pl.divisor = divisor; pl.own = own;
+    pl.in.assign(const_cast<void* const*>(in), const_cast<void* const*>(in) + p);
+    pl.out.assign(out, out + p);
+    return run_plan_once(pl, stream);
+  }
+  return run_fused(in, out, p, n, dtype, divisor, true, own == DDP_OWN_RANK ? 1 : 0,
+                   algo == DDP_ALGO_FUSED, stream);
+}
+
+ddp_status ddp_allgather(const void* const* in, void* const* out, int32_t p, int64_t m, ddp_dtype dtype,
+                         ddp_own own, ddp_algo algo, cudaStream_t stream) {
+  DDP_TRY(check_common(p, m, dtype));
+  DDP_TRY(check_algo(algo));
+  DDP_TRY(check_own(own));
+  DDP_TRY(check_ptrs(in, p, "in"));
+  DDP_TRY(check_ptrs(const_cast<const void* const*>(out), p, "out"));
+  const int es = esize(dtype);
+  std::vector<std::pair<uintptr_t, uintptr_t>> outs, all;
+  for (int r = 0; r < p; ++r) outs.push_back(range_of(out[r], static_cast<int64_t>(p) * m * es));
+  DDP_CHECK(disjoint(outs), DDP_ERR_ARG, "output buffers overlap");
+  for (int r = 0; r < p; ++r) {
+    all = outs;
+    all.push_back(range_of(in[r], m * es));
+    DDP_CHECK(disjoint(all), DDP_ERR_ARG, "an output buffer overlaps an input");
+  }
+  if (m == 0) return DDP_OK;
+  if (algo == DDP_ALGO_RING_STEPS) {
+    Plan pl;
+    pl.op = DDP_OP_ALLGATHER; pl.p = p; pl.n = m; pl.dt = dtype; pl.own = own;
+    pl.in.assign(const_cast<void* const*>(in), const_cast<void* const*>(in) + p);
+    pl.out.assign(out, out + p);
+    return run_plan_once(pl, stream);
+  }
+  FanoutArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int c = 0; c < p; ++c) {
+    const int holder = (own == DDP_OWN_RANK) ? c : (c + p - 1) % p;
+    a.src[c] = static_cast<const char*>(in[holder]);
+    a.job_off[c] = static_cast<int64_t>(c) * m * es;
+  }
+  for (int r = 0; r < p; ++r) a.dst[r] = static_cast<char*>(out[r]);
+  a.nbytes = m * es;
+  a.njobs = p;
+  a.ndst = p;
+  DDP_CUDA(launch_fanout(a, stream), "all-gather launch");
+  return DDP_OK;
+}
+
+ddp_status ddp_broadcast(void* const* bufs, int32_t p, int64_t nbytes, int32_t root, ddp_algo algo,
+                         cudaStream_t stream) {
+  DDP_TRY(check_common(p, nbytes, DDP_FLOAT32));
+  DDP_TRY(check_algo(algo));
+  DDP_CHECK(root >= 0 && root < p, DDP_ERR_ARG, "root out of range");
+  DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
+  std::vector<std::pair<uintptr_t, uintptr_t>> rg;
+  for (int r = 0; r < p; ++r) rg.push_back(range_of(bufs[r], nbytes));
+  DDP_CHECK(disjoint(rg), DDP_ERR_ARG, "replica buffers overlap");
+  if (nbytes == 0 || p == 1) return DDP_OK;
+  if (algo == DDP_ALGO_RING_STEPS) {
+    Plan pl;
+    pl.op = DDP_OP_BROADCAST; pl.p = p; pl.n = nbytes; pl.root = root;
+    pl.in.assign(bufs, bufs + p);
+    return run_plan_once(pl, stream);
+  }
+  FanoutArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.src[0] = static_cast<const char*>(bufs[root]);
+  int q = 0;
+  for (int r = 0; r < p; ++r)
+    if (r != root) a.dst[q++] = static_cast<char*>(bufs[r]);
+  a.nbytes = nbytes;
+  a.njobs = 1;
+  a.ndst = q;
+  DDP_CUDA(launch_fanout(a, stream), "broadcast launch");
+  return DDP_OK;
+}
+
+ddp_status ddp_broadcast_coalesced(int32_t p, int32_t k, void* const* tensors, const int64_t* nbytes,
+                                   int32_t root, int64_t bucket_cap_bytes, ddp_algo algo,
+                                   cudaStream_t stream) {
+  DDP_TRY(check_common(p, 0, DDP_FLOAT32));
+  DDP_TRY(check_algo(algo));
+  DDP_CHECK(k >= 0, DDP_ERR_ARG, "k must be >= 0");
+  DDP_CHECK(root >= 0 && root < p, DDP_ERR_ARG, "root out of range");
+  DDP_CHECK(bucket_cap_bytes >= 0, DDP_ERR_ARG, "bucket_cap_bytes must be >= 0");
+  if (k == 0) return DDP_OK;
+  DDP_CHECK(tensors && nbytes, DDP_ERR_ARG, "tensors / nbytes arrays are null");
+  std::vector<std::pair<uintptr_t, uintptr_t>> rg;
+  for (int32_t j = 0; j < k; ++j) {
+    DDP_CHECK(nbytes[j] >= 0, DDP_ERR_ARG, "nbytes must be >= 0");
+    if (nbytes[j] == 0) continue;
+    for (int32_t r = 0; r < p; ++r) {
+      const void* t = tensors[static_cast<int64_t>(r) * k + j];
+      DDP_CHECK(t != nullptr, DDP_ERR_ARG, "tensors[" + std::to_string(r * k + j) + "] is null");
+      rg.push_back(range_of(t, nbytes[j]));
+    }
+  }
+  DDP_CHECK(disjoint(rg), DDP_ERR_ARG, "tensors overlap");
+  if (p == 1) return DDP_OK;
+  const int64_t cap = bucket_cap_bytes > 0 ? bucket_cap_bytes : int64_t(250) * 1024 * 1024;
+  auto T = [&](int r, int j) { return tensors[static_cast<int64_t>(r) * k + j]; };
+
+  if (algo != DDP_ALGO_RING_STEPS) {
+    // Every root tensor straight to the p-1 other replicas, kFanD destinations per launch.
+    const int ndst = p - 1;
+    const int per_launch = std::max(1, std::min(kFanT, kFanD / ndst));
+    MultiFanoutArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.ndst = ndst;
+    auto flush = [&]() -> ddp_status {
+      if (a.ntensors == 0) return DDP_OK;
+      DDP_CUDA(launch_multi_fanout(a, stream), "coalesced broadcast launch");
+      std::memset(&a, 0, sizeof(a));
+      a.ndst = ndst;
+      return DDP_OK;
+    };
+    for (int32_t j = 0; j < k; ++j) {
+      if (nbytes[j] == 0) continue;
+      const int64_t tiles = (nbytes[j] + kSegTileBytes - 1) / kSegTileBytes;
+      if (a.ntensors == per_launch || static_cast<int64_t>(a.tile0[a.ntensors]) + tiles > 0x7FFFFFFF)
+        DDP_TRY(flush());
+      const int t = a.ntensors;
+      a.src[t] = static_cast<const char*>(T(root, j));
+      a.bytes[t] = nbytes[j];
+      int q = 0;
+      for (int r = 0; r < p; ++r)
+        if (r != root) a.dst[t * ndst + q++] = static_cast<char*>(T(r, j));
+      a.tile0[t + 1] = a.tile0[t] + static_cast<int32_t>(tiles);
+      ++a.ntensors;
+    }
+    return flush();
+  }
+
+  // Literal: coalesce into buckets of at most `cap` bytes; per bucket pack on
+  // the root, broadcast the packed buffer by the doubling tree, unpack.
+  std::vector<std::vector<int32_t>> groups;
+  std::vector<int64_t> gbytes;
+  {
+    std::vector<int32_t> cur;
+    int64_t size = 0;
+    for (int32_t j = 0; j < k; ++j) {
+      if (!cur.empty() && size + nbytes[j] > cap) {
+        groups.push_back(cur);
+        gbytes.push_back(size);
+        cur.clear();
+        size = 0;
+      }
+      cur.push_back(j);
+      size += nbytes[j];
+    }
+    if (!cur.empty()) { groups.push_back(cur); gbytes.push_back(size); }
+  }
+  const int64_t gmax = *std::max_element(gbytes.begin(), gbytes.end());
+  if (gmax == 0) return DDP_OK;
+  const int64_t slot = (gmax + 255) / 256 * 256;
+  void* wsv = nullptr;
+  DDP_CUDA(cudaMallocAsync(&wsv, slot * p, stream), "broadcast workspace allocation");
+  char* ws = static_cast<char*>(wsv);
+  ddp_status rc = DDP_OK;
+  for (size_t g = 0; g < groups.size() && rc == DDP_OK; ++g) {
+    if (gbytes[g] == 0) continue;
+    SegBatcher pack(DDP_FLOAT32, 1.0f, stream);
+    int64_t pos = 0;
+    for (int32_t j : groups[g]) {
+      rc = pack.add(T(root, j), ws + root * slot + pos, nbytes[j]);
+      if (rc != DDP_OK) break;
+      pos += nbytes[j];
+    }
+    if (rc == DDP_OK) rc = pack.flush();
+    if (rc != DDP_OK) break;
+    Plan pl;
+    pl.op = DDP_OP_BROADCAST; pl.p = p; pl.n = gbytes[g]; pl.root = root;
+    for (int r = 0; r < p; ++r) pl.in.push_back(ws + r * slot);
+    pl.init();
+    rc = pl.run_all(stream);
+    if (rc != DDP_OK) break;
+    SegBatcher unpack(DDP_FLOAT32, 1.0f, stream);
+    for (int r = 0; r < p && rc == DDP_OK; ++r) {
+      if (r == root) continue;
+      pos = 0;
+      for (int32_t j : groups[g]) {
+        rc = unpack.add(ws + r * slot + pos, T(r, j), nbytes[j]);
+        if (rc != DDP_OK) break;
+        pos += nbytes[j];
+      }
+    }
+    if (rc == DDP_OK) rc = unpack.flush();
+  }
+  const cudaError_t e = cudaFreeAsync(ws, stream);
+  if (rc == DDP_OK && e != cudaSuccess) return cuda_fail(e, "broadcast workspace release");
+  return rc;
+}
+
+ddp_status ddp_ring_create(ddp_ring** handle, ddp_op op, void* const* in, void* const* out, int32_t p,
+                           int64_t n, ddp_dtype dtype, float divisor, ddp_own own, int32_t root,
+                           cudaStream_t stream) {
+  DDP_CHECK(handle != nullptr, DDP_ERR_ARG, "handle pointer is null");
+  *handle = nullptr;
+  DDP_CHECK(op >= DDP_OP_ALLREDUCE && op <= DDP_OP_BROADCAST, DDP_ERR_ARG, "unknown op");
+  DDP_TRY(check_common(p, n, op == DDP_OP_BROADCAST ? DDP_FLOAT32 : dtype));
+  DDP_TRY(check_ptrs(const_cast<const void* const*>(in), p, "in"));
+  const bool needs_out = (op == DDP_OP_REDUCE_SCATTER || op == DDP_OP_ALLGATHER);
+  if (needs_out) DDP_TRY(check_ptrs(const_cast<const void* const*>(out), p, "out"));
+  if (op == DDP_OP_ALLREDUCE || op == DDP_OP_REDUCE_SCATTER) DDP_TRY(check_divisor(divisor));
+  if (op != DDP_OP_BROADCAST) DDP_TRY(check_own(own));
+  if (op == DDP_OP_BROADCAST) DDP_CHECK(root >= 0 && root < p, DDP_ERR_ARG, "root out of range");
+  if (op == DDP_OP_REDUCE_SCATTER && own == DDP_OWN_RANK)
+    DDP_CHECK(n % p == 0, DDP_ERR_NOT_DIVISIBLE,
+              "reduce_scatter: " + std::to_string(n) + " elements are not divisible by " + std::to_string(p) + " ranks");
+  const int es = (op == DDP_OP_BROADCAST) ? 1 : esize(dtype);
+  {
+    std::vector<std::pair<uintptr_t, uintptr_t>> rg;
+    const int64_t in_bytes = n * es;
+    const int64_t out_bytes = (op == DDP_OP_ALLGATHER) ? static_cast<int64_t>(p) * n * es : chunk_size(n, p) * es;
+    for (int r = 0; r < p; ++r) {
+      rg.push_back(range_of(in[r], in_bytes));
+      if (needs_out) rg.push_back(range_of(out[r], out_bytes));
+    }
+    DDP_CHECK(disjoint(rg), DDP_ERR_ARG, "buffers overlap");
+  }
+  ddp_ring* h = new ddp_ring();
+  Plan& pl = h->plan;
+  pl.op = op; pl.p = p; pl.n = n; pl.dt = dtype; pl.divisor = divisor; pl.own = own; pl.root = root;
+  pl.in.assign(in, in + p);
+  if (needs_out) pl.out.assign(out, out + p);
+  pl.init();
+  if (n == 0) pl.nsteps = 0;
+  h->stream = stream;
+  if (pl.needs_ws() && n > 0) {
+    void* w = nullptr;
+    const cudaError_t e = cudaMalloc(&w, pl.ws_elems() * sizeof(float));
+    if (e != cudaSuccess) {
+      delete h;
+      t_error = std::string("handle workspace allocation: ") + cudaGetErrorString(e);
+      return DDP_ERR_NOMEM;
+    }
+    pl.ws = static_cast<float*>(w);
+  }
+  *handle = h;
+  return DDP_OK;
+}
+
+int32_t ddp_ring_num_steps(const ddp_ring* h) { return h ? h->plan.nsteps : -1; }
+int32_t ddp_ring_steps_done(const ddp_ring* h) { return h ? h->plan.done : -1; }
+
+ddp_status ddp_ring_step(ddp_ring* h) {
+  DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
+  return h->plan.step(h->stream);
+}
+
+ddp_status ddp_ring_workspace(const ddp_ring* h, void** fp32_partials, int64_t* elems_per_slot) {
+  DDP_CHECK(h && fp32_partials && elems_per_slot, DDP_ERR_ARG, "null argument");
+  *fp32_partials = h->plan.ws;
+  *elems_per_slot = h->plan.ws ? h->plan.cs : 0;
+  return DDP_OK;
+}
+
+ddp_status ddp_ring_bytes_sent(const ddp_ring* h, int32_t rank, int64_t* bytes) {
+  DDP_CHECK(h && bytes, DDP_ERR_ARG, "null argument");
+  DDP_CHECK(rank >= 0 && rank < h->plan.p, DDP_ERR_ARG, "rank out of range");
+  *bytes = h->plan.sent[rank];
+  return DDP_OK;
+}
+
+ddp_status ddp_ring_sync(ddp_ring* h) {
+  DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
+  int32_t code = 0;
+  return ddp_device_error(h->stream, &code);
+}
+
+ddp_status ddp_ring_destroy(ddp_ring* h) {
+  if (!h) return DDP_OK;
+  cudaError_t e = cudaSuccess;
+  if (h->plan.ws) e = cudaFree(h->plan.ws);
+  delete h;
+  if (e != cudaSuccess) return cuda_fail(e, "handle workspace release");
+  return DDP_OK;
+}
+
+ddp_status ddp_device_error(cudaStream_t stream, int32_t* code) {
+  DDP_CHECK(code != nullptr, DDP_ERR_ARG, "code pointer is null");
+  int v = 0;
+  DDP_CUDA(read_device_error(stream, &v), "device status read");
+  *code = v;
+  if (v != 0) return fail(DDP_ERR_TIMEOUT, "a kernel gave up a bounded wait (code " + std::to_string(v) + ")");
+  return DDP_OK;
+}
+
+int64_t ddp_kernel_launches(void) { return launches(); }
+
+const char* ddp_last_error(void) { return t_error.c_str(); }
+
+const char* ddp_status_string(ddp_status s) {
+  switch (s) {
+    case DDP_OK: return "DDP_OK";
+    case DDP_ERR_ARG: return "DDP_ERR_ARG";
+    case DDP_ERR_DTYPE: return "DDP_ERR_DTYPE";
+    case DDP_ERR_NOT_DIVISIBLE: return "DDP_ERR_NOT_DIVISIBLE";
+    case DDP_ERR_ALIGN: return "DDP_ERR_ALIGN";
+    case DDP_ERR_NOMEM: return "DDP_ERR_NOMEM";
+    case DDP_ERR_CUDA: return "DDP_ERR_CUDA";
+    case DDP_ERR_TIMEOUT: return "DDP_ERR_TIMEOUT";
+    case DDP_ERR_STATE: return "DDP_ERR_STATE";
+  }
+  return "DDP_ERR_UNKNOWN";
+}
+
+}  // extern "C"

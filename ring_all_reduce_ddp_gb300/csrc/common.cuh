@@ -1,0 +1,136 @@
+// Device helpers and kernel argument blocks shared by the library's kernels.
+//
+// Arithmetic rules of the whole library: a sum of p contributions is a left
+// fold of IEEE round-to-nearest fp32 additions (__fadd_rn, never contracted or
+// reassociated), the scale is one IEEE division (__fdiv_rn), bf16 values are
+// widened exactly (bits << 16) and narrowed once with round-to-nearest-even.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ddp_ring.h"
+
+namespace ddp {
+
+constexpr int kThreads = 256;
+constexpr int kMaxP = DDP_MAX_P;
+
+// ---------------------------------------------------------------- elements
+__device__ __forceinline__ float widen(float x) { return x; }
+__device__ __forceinline__ float widen(__nv_bfloat16 x) {
+  return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(x)) << 16);
+}
+
+template <typename T> __device__ __forceinline__ T narrow(float x);
+template <> __device__ __forceinline__ float narrow<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 narrow<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// A 16-byte vector seen as N fp32 lanes.
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                      __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+};
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void unpack2(uint32_t w, float* f) {
+    f[0] = __uint_as_float(w << 16);          // element 2i: low half (little endian)
+    f[1] = __uint_as_float(w & 0xFFFF0000u);  // element 2i+1: high half
+  }
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    unpack2(v.x, f); unpack2(v.y, f + 2); unpack2(v.z, f + 4); unpack2(v.w, f + 6);
+  }
+  __device__ __forceinline__ static uint32_t pack2(float a, float b) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+  }
+};
+
+// ------------------------------------------------------------ argument blocks
+
+// Fused one-pass reduction (all-reduce, reduce-scatter).
+// src holds the p input replicas twice over (src[j] = replica j mod p), so the
+// ring order of chunk c, replicas o, o+1, ..., o+p-1 (mod p) with origin o,
+// is src[o .. o+p-1] without a modulo.
+struct FusedArgs {
+  const void* src[2 * kMaxP];
+  void* dst[kMaxP];  // all-reduce: the p replicas; reduce-scatter: out[rank]
+  int64_t n;         // elements per input replica
+  int64_t cs;        // chunk size, ceil(n / p)
+  float divisor;
+  int p;
+  int scatter;       // 0: write y to every dst at index i; 1: to dst[owner] at i - c*cs
+  int shift;         // origin of chunk c is (c + shift) mod p
+  int same_align;    // every src / dst base has the same address mod 16
+};
+
+// Literal reduce-scatter step. x[r]: replica r's input (const except in the
+// fp32 in-place all-reduce); w: fp32 partials [2][p][cs]; out[d]: where the
+// last step writes (at chunk-relative index if out_rel, else at i).
+struct RingStepArgs {
+  void* x[kMaxP];
+  void* out[kMaxP];
+  float* w;
+  int64_t n, cs;
+  float divisor;
+  int p, step, shift, last, out_rel;
+};
+
+// Copy jobs: job j copies nbytes[j] bytes from src[j] to dst[j].
+struct PairCopyArgs {
+  const char* src[kMaxP];
+  char* dst[kMaxP];
+  int64_t nbytes[kMaxP];
+  int njobs;
+};
+
+// Fan-out: job j copies nbytes from src[j] to every dst[q] + job_off[j].
+struct FanoutArgs {
+  const char* src[kMaxP];
+  int64_t job_off[kMaxP];
+  char* dst[kMaxP];
+  int64_t nbytes;
+  int njobs, ndst;
+};
+
+// Segment copy (multi-tensor): segment s copies bytes[s] bytes from src[s] to
+// dst[s]; tile0 is the prefix sum of each segment's tile count.
+constexpr int kSegCap = 512;
+constexpr int kSegTileBytes = 16384;
+struct SegCopyArgs {
+  const char* src[kSegCap];
+  char* dst[kSegCap];
+  int64_t bytes[kSegCap];
+  int32_t tile0[kSegCap + 1];
+  int nseg;
+  int elem_size;     // for the dividing copy
+  float predivide;   // 1: plain byte copy
+};
+
+// Multi-tensor fan-out (coalesced broadcast): tensor t goes from src[t] to
+// dst[t * ndst + q] for q < ndst.
+constexpr int kFanT = 64;
+constexpr int kFanD = 1024;
+struct MultiFanoutArgs {
+  const char* src[kFanT];
+  int64_t bytes[kFanT];
+  int32_t tile0[kFanT + 1];
+  char* dst[kFanD];
+  int ntensors, ndst;
+};
+
+}  // namespace ddp

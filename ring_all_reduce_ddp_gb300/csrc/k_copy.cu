@@ -1,0 +1,185 @@
+// Copy kernels: ring all-gather steps and doubling-tree broadcast steps (copy
+// jobs), the fused all-gather and broadcast (one read, many writes), bucket
+// flatten / unflatten (segment copies, optionally dividing), and the coalesced
+// broadcast (multi-tensor fan-out).
+//
+// Sources: "Data parallelism", "Ring all-reduce, derived" (all-gather: the
+// receiver overwrites its copy); "Collective Ops From Scratch", code/main.py
+// list (doubling-tree broadcast, N-1 rotations for all-gather); "PyTorch DDP
+// Deep Dive", Part 2 (mark_variable_ready copies each gradient into its bucket
+// slice, pre-dividing; finalize_backward copies back; _broadcast_coalesced
+// flattens, broadcasts and unflattens).
+//
+// Every copy picks the widest word (16, 8, 4, 2 or 1 bytes) on which source
+// and destination agree modulo its size, copies the bytes before the first
+// boundary and after the last one singly, and the words in between.
+#include "launch.h"
+
+namespace ddp {
+namespace {
+
+constexpr int kWordsInFlight = 4;
+constexpr int64_t kTileBytes = kSegTileBytes;  // = kThreads * 16 bytes * kWordsInFlight
+
+template <typename W>
+__device__ __forceinline__ void copy_words(const char* s, char* const* d, int nd, int64_t nbytes,
+                                           int tid, int nthr) {
+  constexpr int64_t w = sizeof(W);
+  int64_t head = static_cast<int64_t>((w - (reinterpret_cast<uintptr_t>(s) & (w - 1))) & (w - 1));
+  if (head > nbytes) head = nbytes;
+  const int64_t nw = (nbytes - head) / w;
+  const int64_t tail0 = head + nw * w;
+  for (int64_t b = tid; b < head; b += nthr) {
+    const char v = s[b];
+    for (int q = 0; q < nd; ++q) d[q][b] = v;
+  }
+  for (int64_t b = tail0 + tid; b < nbytes; b += nthr) {
+    const char v = s[b];
+    for (int q = 0; q < nd; ++q) d[q][b] = v;
+  }
+  const W* sw = reinterpret_cast<const W*>(s + head);
+  for (int64_t k0 = tid; k0 < nw; k0 += static_cast<int64_t>(nthr) * kWordsInFlight) {
+    W v[kWordsInFlight];
+#pragma unroll
+    for (int u = 0; u < kWordsInFlight; ++u) {
+      const int64_t k = k0 + static_cast<int64_t>(u) * nthr;
+      if (k < nw) v[u] = sw[k];
+    }
+    for (int q = 0; q < nd; ++q) {
+      W* dw = reinterpret_cast<W*>(d[q] + head);
+#pragma unroll
+      for (int u = 0; u < kWordsInFlight; ++u) {
+        const int64_t k = k0 + static_cast<int64_t>(u) * nthr;
+        if (k < nw) dw[k] = v[u];
+      }
+    }
+  }
+}
+
+// Copy nbytes from s to each of the nd destinations d[q] (one read, nd writes).
+__device__ __forceinline__ void copy_to_all(const char* s, char* const* d, int nd, int64_t nbytes,
+                                            int tid, int nthr) {
+  uintptr_t x = 0;
+  for (int q = 0; q < nd; ++q) x |= reinterpret_cast<uintptr_t>(s) ^ reinterpret_cast<uintptr_t>(d[q]);
+  if ((x & 15) == 0) copy_words<uint4>(s, d, nd, nbytes, tid, nthr);
+  else if ((x & 7) == 0) copy_words<uint2>(s, d, nd, nbytes, tid, nthr);
+  else if ((x & 3) == 0) copy_words<uint32_t>(s, d, nd, nbytes, tid, nthr);
+  else if ((x & 1) == 0) copy_words<uint16_t>(s, d, nd, nbytes, tid, nthr);
+  else copy_words<uint8_t>(s, d, nd, nbytes, tid, nthr);
+}
+
+// ---------------------------------------------------------------- kernels
+__global__ void __launch_bounds__(kThreads) k_pair_copy(const __grid_constant__ PairCopyArgs a) {
+  const int j = blockIdx.y;
+  const int64_t nb = a.nbytes[j];
+  const int64_t ntiles = (nb + kTileBytes - 1) / kTileBytes;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t b0 = t * kTileBytes;
+    const int64_t len = min(kTileBytes, nb - b0);
+    char* d = a.dst[j] + b0;
+    copy_to_all(a.src[j] + b0, &d, 1, len, threadIdx.x, blockDim.x);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_fanout(const __grid_constant__ FanoutArgs a) {
+  const int j = blockIdx.y;
+  const int64_t ntiles = (a.nbytes + kTileBytes - 1) / kTileBytes;
+  __shared__ char* dst[kMaxP];
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t b0 = t * kTileBytes;
+    const int64_t len = min(kTileBytes, a.nbytes - b0);
+    __syncthreads();
+    for (int q = threadIdx.x; q < a.ndst; q += blockDim.x) dst[q] = a.dst[q] + a.job_off[j] + b0;
+    __syncthreads();
+    copy_to_all(a.src[j] + b0, dst, a.ndst, len, threadIdx.x, blockDim.x);
+  }
+}
+
+__device__ __forceinline__ int find_tile_owner(const int32_t* tile0, int nseg, int32_t b) {
+  int lo = 0, hi = nseg;  // tile0[lo] <= b < tile0[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile0[mid] <= b) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_seg_copy(const __grid_constant__ SegCopyArgs a) {
+  const int32_t b = blockIdx.x;
+  const int s = find_tile_owner(a.tile0, a.nseg, b);
+  const int64_t b0 = static_cast<int64_t>(b - a.tile0[s]) * kSegTileBytes;
+  const int64_t len = min(static_cast<int64_t>(kSegTileBytes), a.bytes[s] - b0);
+  if (len <= 0) return;
+  const char* src = a.src[s] + b0;
+  char* dst = a.dst[s] + b0;
+  if (a.predivide == 1.0f) {
+    copy_to_all(src, &dst, 1, len, threadIdx.x, blockDim.x);
+  } else {
+    const T* xs = reinterpret_cast<const T*>(src);
+    T* xd = reinterpret_cast<T*>(dst);
+    const int64_t ne = len / static_cast<int64_t>(sizeof(T));
+    for (int64_t e = threadIdx.x; e < ne; e += blockDim.x)
+      xd[e] = narrow<T>(__fdiv_rn(widen(xs[e]), a.predivide));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_multi_fanout(const __grid_constant__ MultiFanoutArgs a) {
+  const int32_t b = blockIdx.x;
+  const int t = find_tile_owner(a.tile0, a.ntensors, b);
+  const int64_t b0 = static_cast<int64_t>(b - a.tile0[t]) * kTileBytes;
+  const int64_t len = min(kTileBytes, a.bytes[t] - b0);
+  if (len <= 0) return;
+  __shared__ char* dst[kFanD];
+  for (int q = threadIdx.x; q < a.ndst; q += blockDim.x) dst[q] = a.dst[t * a.ndst + q] + b0;
+  __syncthreads();
+  copy_to_all(a.src[t] + b0, dst, a.ndst, len, threadIdx.x, blockDim.x);
+}
+
+int grid_x_for(int64_t tiles, int rows) {
+  const int64_t target = static_cast<int64_t>(sm_count()) * (2048 / kThreads);
+  int64_t bx = (target + rows - 1) / rows;
+  if (bx > tiles) bx = tiles;
+  if (bx < 1) bx = 1;
+  return static_cast<int>(bx);
+}
+
+}  // namespace
+
+cudaError_t launch_pair_copy(const PairCopyArgs& a, cudaStream_t s) {
+  if (a.njobs <= 0) return cudaSuccess;
+  int64_t maxb = 0;
+  for (int j = 0; j < a.njobs; ++j) maxb = a.nbytes[j] > maxb ? a.nbytes[j] : maxb;
+  if (maxb == 0) return cudaSuccess;
+  const dim3 grid(grid_x_for((maxb + kTileBytes - 1) / kTileBytes, a.njobs), a.njobs);
+  k_pair_copy<<<grid, kThreads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s) {
+  if (a.njobs <= 0 || a.nbytes <= 0 || a.ndst <= 0) return cudaSuccess;
+  const dim3 grid(grid_x_for((a.nbytes + kTileBytes - 1) / kTileBytes, a.njobs), a.njobs);
+  k_fanout<<<grid, kThreads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seg_copy(const SegCopyArgs& a, ddp_dtype dt, cudaStream_t s) {
+  const int32_t ntiles = a.tile0[a.nseg];
+  if (a.nseg <= 0 || ntiles <= 0) return cudaSuccess;
+  if (dt == DDP_BFLOAT16) k_seg_copy<__nv_bfloat16><<<ntiles, kThreads, 0, s>>>(a);
+  else k_seg_copy<float><<<ntiles, kThreads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_multi_fanout(const MultiFanoutArgs& a, cudaStream_t s) {
+  const int32_t ntiles = a.tile0[a.ntensors];
+  if (a.ntensors <= 0 || ntiles <= 0 || a.ndst <= 0) return cudaSuccess;
+  k_multi_fanout<<<ntiles, kThreads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace ddp

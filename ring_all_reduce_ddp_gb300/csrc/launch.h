@@ -1,0 +1,24 @@
+// Host-side launchers of the library's kernels (internal interface between the
+// C ABI in api.cu and the kernel translation units).
+#pragma once
+
+#include "common.cuh"
+
+namespace ddp {
+
+int sm_count();               // SMs of the current device (cached per device)
+void count_launch();          // one more kernel launched by this library
+int64_t launches();
+
+cudaError_t launch_fused_reduce(const FusedArgs& a, ddp_dtype dt, bool staged, cudaStream_t s);
+cudaError_t launch_rs_step_inplace_f32(const RingStepArgs& a, cudaStream_t s);
+cudaError_t launch_rs_step_ws(const RingStepArgs& a, ddp_dtype dt, cudaStream_t s);
+cudaError_t launch_pair_copy(const PairCopyArgs& a, cudaStream_t s);
+cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s);
+cudaError_t launch_seg_copy(const SegCopyArgs& a, ddp_dtype dt, cudaStream_t s);
+cudaError_t launch_multi_fanout(const MultiFanoutArgs& a, cudaStream_t s);
+
+// Synchronize s, then read and clear the device error word.
+cudaError_t read_device_error(cudaStream_t s, int* code);
+
+}  // namespace ddp

@@ -1,0 +1,93 @@
+"""The C-ABI library builds, loads and exports every symbol include/*.h declares;
+its host-only planner matches the oracle (CPU only, no CUDA calls)."""
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+from synth import shapes
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from ring_all_reduce_ddp_gb300 import build
+    build.build_library()
+    import ring_all_reduce_ddp_gb300 as d
+    return d
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(ddp_\w+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = _declared()
+    assert declared, "no declarations found"
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (ddp_\w+)", out))
+    assert declared <= exported, declared - exported
+    # and the binding knows every one of them, under the same name
+    assert declared <= set(L.exported_symbols())
+    for name in declared:
+        assert hasattr(L.lib(), name)
+
+
+def test_status_strings(L):
+    assert L.status_string(L.DDP_OK) == "DDP_OK"
+    assert L.status_string(L.DDP_ERR_NOT_DIVISIBLE) == "DDP_ERR_NOT_DIVISIBLE"
+
+
+@pytest.mark.parametrize("builder,esize", [(shapes.tiny, 4), (shapes.resnet50, 4), (shapes.gpt2_small, 4),
+                                            (shapes.llama_1b, 2)])
+@pytest.mark.parametrize("order", ["reversed", "registration"])
+def test_bucket_assign_matches_oracle(L, builder, esize, order):
+    from oracle import buckets as ob
+    numel = [shapes.numel(s) for _, s in builder()]
+    first, cap = ((16 << 10), (256 << 10)) if builder is shapes.tiny else ((1 << 20), (25 << 20))
+    want = ob.assign_buckets(numel, esize, first, cap, order)
+    _, off, bn = ob.bucket_layout(numel, want)
+    got = L.ddp_bucket_assign(numel, esize, first, cap,
+                              L.DDP_ORDER_REVERSED if order == "reversed" else L.DDP_ORDER_REGISTRATION)
+    assert got["buckets"] == want
+    assert got["offset"] == off and got["bucket_numel"] == bn
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_bucket_assign_random_edge_cases(L, seed):
+    import numpy as np
+    from oracle import buckets as ob
+    rng = np.random.default_rng(seed)
+    k = int(rng.integers(0, 20))
+    numel = [int(x) for x in rng.integers(0, 50, size=k)]
+    first, cap = int(rng.integers(0, 100)), int(rng.integers(0, 300))
+    for order, code in (("reversed", L.DDP_ORDER_REVERSED), ("registration", L.DDP_ORDER_REGISTRATION)):
+        assert L.ddp_bucket_assign(numel, 4, first, cap, code)["buckets"] == \
+            ob.assign_buckets(numel, 4, first, cap, order)
+
+
+def test_argument_errors_are_reported_before_any_launch(L):
+    with pytest.raises(L.DDPError) as e:
+        L.ddp_bucket_assign([1, -2], 4, 16, 16)
+    assert e.value.status == L.DDP_ERR_ARG
+    lib = L.lib()
+    import ctypes
+    arr = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    assert lib.ddp_allreduce(arr, 0, 10, 0, 1.0, 0, None) == L.DDP_ERR_ARG          # p = 0
+    assert lib.ddp_allreduce(arr, 2, 10, 7, 1.0, 0, None) == L.DDP_ERR_DTYPE        # bad dtype
+    assert lib.ddp_allreduce(arr, 2, 10, 0, 0.0, 0, None) == L.DDP_ERR_ARG          # divisor 0
+    assert lib.ddp_allreduce(arr, 2, 2000, 0, 1.0, 0, None) == L.DDP_ERR_ARG        # overlap
+    assert "overlap" in L.ddp_last_error()
+    assert lib.ddp_reduce_scatter(arr, (ctypes.c_void_p * 2)(0x10000, 0x20000), 2, 11, 0, 1.0,
+                                  L.DDP_OWN_RANK, 0, None) == L.DDP_ERR_NOT_DIVISIBLE
+    assert lib.ddp_broadcast(arr, 2, 16, 5, 0, None) == L.DDP_ERR_ARG                # root out of range
+    # zero-size work is a no-op that touches no device
+    assert lib.ddp_allreduce(arr, 2, 0, 0, 1.0, 0, None) == L.DDP_OK

@@ -1,0 +1,283 @@
+"""GPU parity of the DDP path: bucket flatten / unflatten, the literal schedule
+step by step (state after every step, bytes on the wire), and whole gradient
+synchronisations on the four gradient sets, against the CPU oracle.
+
+Full-size sets are checked on sampled elements (every chunk and tensor
+boundary +-2, the first and last 64 elements of each bucket, and random
+indices), each computed by the oracle's own ring simulation restricted to
+those elements, from inputs regenerated on the host by the seeded generator."""
+import numpy as np
+import pytest
+
+import ring_all_reduce_ddp_gb300 as D
+from oracle import buckets as ob
+from oracle import ring as orc
+from oracle.bf16 import bf16_to_f32
+from ring_all_reduce_ddp_gb300.reducer import Reducer, broadcast_buffers
+from synth import workloads as W
+from tests.helpers import assert_bf16_close, assert_bit_equal, make_replicas, to_host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": D.DDP_FLOAT32, "bf16": D.DDP_BFLOAT16}
+
+
+# ------------------------------------------------------------ flatten / unflatten
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("predivide", [1.0, 4.0, 3.0])
+def test_flatten_unflatten_tiny(dtype, predivide):
+    cfg = dict(W.CONFIGS["tiny"], dtype=dtype)
+    p = cfg["p"]
+    grads, _ = W.make_grads(cfg)
+    numel = W.numels(cfg)
+    starts = W.tensor_starts(cfg)
+    plan = ob.assign_buckets(numel, W.esize(cfg), cfg["first_cap"], cfg["cap"])
+    _, offset, bnumel = ob.bucket_layout(numel, plan)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    for b, members in enumerate(plan):
+        flat = [torch.full((bnumel[b],), 5.0, dtype=tdt, device="cuda") for _ in range(p)]
+        D.ddp_bucket_flatten([[grads[r][t] for t in members] for r in range(p)], [numel[t] for t in members],
+                             [offset[t] for t in members], flat, DT[dtype], predivide)
+        for r in range(p):
+            host = {t: W.host_values(cfg, r, np.arange(starts[t], starts[t] + numel[t])) for t in members}
+            if dtype == "f32":
+                want = ob.flatten([host.get(t, np.zeros(0, np.float32)) for t in range(len(numel))], members,
+                                  offset, bnumel[b], predivide)
+            else:
+                from oracle.bf16 import f32_to_bf16
+                wide = [bf16_to_f32(host[t]) if t in host else np.zeros(0, np.float32) for t in range(len(numel))]
+                want = f32_to_bf16(ob.flatten(wide, members, offset, bnumel[b], predivide))
+            assert_bit_equal(to_host(flat[r]), want, f"bucket {b} replica {r}")
+        # unflatten into fresh tensors gives the flat slices back
+        outs = [[torch.zeros(numel[t], dtype=tdt, device="cuda") for t in members] for _ in range(p)]
+        D.ddp_bucket_unflatten(flat, [numel[t] for t in members], [offset[t] for t in members], outs, DT[dtype])
+        for r in range(p):
+            fh = to_host(flat[r])
+            back = ob.unflatten(fh, members, offset, numel)
+            for j, t in enumerate(members):
+                assert_bit_equal(to_host(outs[r][j]), back[t], f"tensor {t}")
+
+
+# ---------------------------------------------------------- literal schedule
+@pytest.mark.parametrize("p,n", [(1, 1000), (2, 17), (3, 1000), (4, 277421), (5, 4), (8, 65541), (13, 20011)])
+def test_allreduce_steps_fp32_state_after_every_step(p, n):
+    devs, hosts, _ = make_replicas(p, n, "f32", "normal", seed=400 + p)
+    want, info = orc.allreduce(hosts, n, float(p), "f32", snapshots=True)
+    with D.DDPRing(D.DDP_OP_ALLREDUCE, devs, None, n, D.DDP_FLOAT32, float(p)) as ring:
+        assert ring.num_steps() == len(info["snapshots"]) == (1 if p == 1 else 2 * (p - 1))
+        for s in range(ring.num_steps()):
+            ring.step()
+            ring.sync()
+            for r in range(p):
+                assert_bit_equal(to_host(devs[r]), info["snapshots"][s][r][:n], f"step {s} rank {r}")
+        for r in range(p):
+            assert ring.bytes_sent(r) == info["bytes_sent"][r]
+        with pytest.raises(D.DDPError) as e:
+            ring.step()
+        assert e.value.status == D.DDP_ERR_STATE
+
+
+@pytest.mark.parametrize("p,n", [(2, 1001), (4, 277421), (8, 65541)])
+def test_allreduce_steps_bf16_partials_in_fp32_workspace(p, n):
+    devs, hosts, _ = make_replicas(p, n, "bf16", "normal", seed=500 + p)
+    want, info = orc.allreduce(hosts, n, float(p), "bf16", snapshots=True)
+    cs = info["cs"]
+    with D.DDPRing(D.DDP_OP_ALLREDUCE, devs, None, n, D.DDP_BFLOAT16, float(p)) as ring:
+        ws_ptr, slot = ring.workspace()
+        assert ws_ptr and slot == cs
+        for s in range(ring.num_steps()):
+            ring.step()
+            ring.sync()
+            snap = info["snapshots"][s]
+            if s < p - 2:  # the partial rank d just received is in slot d of half s & 1
+                host_ws = _read_f32(ws_ptr, 2 * p * cs)
+                for d in range(p):
+                    c = (d - 1 - s) % p
+                    lo, hi = c * cs, min(n, (c + 1) * cs)
+                    base = ((s & 1) * p + d) * cs
+                    assert_bit_equal(host_ws[base:base + max(0, hi - lo)], snap[d][lo:hi], f"step {s} slot {d}")
+            else:  # finished chunks are in the buffers, the others still hold the inputs
+                done = s - (p - 2)
+                for r in range(p):
+                    got = bf16_to_f32(to_host(devs[r]))
+                    finished = {(r + 1 - j) % p for j in range(done + 1)}
+                    for c in range(p):
+                        lo, hi = c * cs, min(n, (c + 1) * cs)
+                        ref = snap[r][lo:hi] if c in finished else bf16_to_f32(hosts[r][lo:hi])
+                        assert_bit_equal(got[lo:hi], ref, f"step {s} rank {r} chunk {c}")
+        for r in range(p):
+            assert ring.bytes_sent(r) == info["bytes_sent"][r]
+    for r in range(p):
+        assert_bit_equal(to_host(devs[r]), want[r])
+
+
+def _read_f32(ptr, count):
+    """Copy `count` fp32 values at a raw device pointer to the host."""
+    class Raw:
+        __cuda_array_interface__ = {"shape": (count,), "typestr": "<f4", "data": (ptr, False), "version": 2}
+    return torch.as_tensor(Raw(), device="cuda").cpu().numpy().copy()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("own", ["rank", "ring"])
+@pytest.mark.parametrize("p", [1, 2, 4, 7])
+def test_reduce_scatter_and_allgather_handles(p, own, dtype):
+    n = 1001 * p + (0 if own == "rank" else 2)
+    devs, hosts, _ = make_replicas(p, n, dtype, "uniform", seed=600 + p)
+    cs = orc.chunk_size(n, p)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    outs = [torch.zeros(cs, dtype=tdt, device="cuda") for _ in range(p)]
+    code = D.DDP_OWN_RANK if own == "rank" else D.DDP_OWN_RING
+    want, info = orc.reduce_scatter(hosts, n, 2.0, dtype, own)
+    with D.DDPRing(D.DDP_OP_REDUCE_SCATTER, devs, outs, n, DT[dtype], 2.0, code) as ring:
+        assert ring.num_steps() == max(1, p - 1)
+        while ring.steps_done() < ring.num_steps():
+            ring.step()
+        ring.sync()
+        for r in range(p):
+            assert ring.bytes_sent(r) == info["bytes_sent"][r]
+    for r in range(p):
+        assert_bit_equal(to_host(outs[r])[:len(want[r])], want[r], f"rank {r}")
+    if own == "rank" or n % p == 0:
+        m = cs
+        gathered = [torch.zeros(p * m, dtype=tdt, device="cuda") for _ in range(p)]
+        gwant, ginfo = orc.allgather([to_host(o) for o in outs], dtype, own, snapshots=True)
+        with D.DDPRing(D.DDP_OP_ALLGATHER, outs, gathered, m, DT[dtype], 1.0, code) as ring:
+            for s in range(ring.num_steps()):
+                ring.step()
+                ring.sync()
+                if p > 1:
+                    for r in range(p):
+                        g = to_host(gathered[r])
+                        snap = ginfo["snapshots"][s][r]
+                        filled = snap != 0
+                        assert_bit_equal(g[filled], snap[filled], f"all-gather step {s} rank {r}")
+        for r in range(p):
+            assert_bit_equal(to_host(gathered[r]), gwant[r])
+
+
+@pytest.mark.parametrize("p,root", [(2, 0), (5, 2), (8, 7), (9, 0)])
+def test_broadcast_handle_tree_steps(p, root):
+    nbytes = 4099
+    host = [np.full(nbytes, r, dtype=np.uint8) for r in range(p)]
+    devs = [torch.from_numpy(h).cuda() for h in host]
+    want, steps, snaps = orc.broadcast_tree(host, root, snapshots=True)
+    with D.DDPRing(D.DDP_OP_BROADCAST, devs, None, nbytes, root=root) as ring:
+        assert ring.num_steps() == steps
+        for s in range(steps):
+            ring.step()
+            ring.sync()
+            for r in range(p):
+                assert np.array_equal(devs[r].cpu().numpy(), snaps[s][r]), (s, r)
+        sent = [ring.bytes_sent(r) for r in range(p)]
+    assert sum(sent) == (p - 1) * nbytes
+
+
+# ------------------------------------------------------------- whole syncs
+def _sample(n, cs_p, tensor_bounds, rng, k=2000):
+    idx = set(range(min(n, 64))) | set(range(max(0, n - 64), n))
+    p = cs_p[1]
+    cs = cs_p[0]
+    for c in range(p + 1):
+        for d in (-2, -1, 0, 1, 2):
+            i = c * cs + d
+            if 0 <= i < n:
+                idx.add(i)
+    for b in tensor_bounds:
+        for d in (-2, -1, 0, 1, 2):
+            if 0 <= b + d < n:
+                idx.add(b + d)
+    idx |= set(int(x) for x in rng.integers(0, n, size=min(k, n)))
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+def _check_sync_sampled(cfg, red, grads, rng, per_bucket=2000):
+    """Compare the synchronised gradients with the oracle on sampled elements of every bucket."""
+    p = cfg["p"]
+    starts = W.tensor_starts(cfg)
+    numel = W.numels(cfg)
+    Dv = W.divisor(cfg)
+    for b, members in enumerate(red.buckets):
+        n = red.bucket_numel[b]
+        offs = [red.offset[t] for t in members]
+        idx = _sample(n, (orc.chunk_size(n, p), p), offs, rng, per_bucket)
+        # element i of the bucket is element i - offset[t] of tensor t
+        which = np.searchsorted(np.array(offs), idx, side="right") - 1
+        tens = np.array(members)[which]
+        within = idx - np.array(offs)[which]
+        flat_idx = np.array(starts)[tens] + within
+        ins = [W.host_values(cfg, r, flat_idx) for r in range(p)]
+        want, _ = orc.allreduce(ins, n, Dv, cfg["dtype"], idx=idx)
+        for r in range(p):
+            got = np.empty(idx.size, dtype=want[r].dtype)
+            for t in np.unique(tens):
+                sel = tens == t
+                vals = grads[r][t].view(-1)[torch.from_numpy(within[sel]).cuda()]
+                got[sel] = to_host(vals)
+            assert_bit_equal(got, want[r], f"bucket {b} replica {r}")
+            if cfg["dtype"] == "bf16":
+                assert_bf16_close(got, want[r])
+    return True
+
+
+@pytest.mark.parametrize("algo", [D.DDP_ALGO_FUSED, D.DDP_ALGO_RING_STEPS])
+def test_tiny_ddp_sync_full_parity(algo):
+    """Ten odd-sized tensors, p = 4: flatten, all-reduce, unflatten; every element."""
+    cfg = W.CONFIGS["tiny"]
+    p = cfg["p"]
+    grads, _ = W.make_grads(cfg)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    assert red.buckets == [[9, 8], [7, 6, 5, 4, 3, 2, 1, 0]]
+    red.sync_gradients(W.divisor(cfg), algo)
+    torch.cuda.synchronize()
+    numel = W.numels(cfg)
+    starts = W.tensor_starts(cfg)
+    for b, members in enumerate(red.buckets):
+        n = red.bucket_numel[b]
+        ins = []
+        for r in range(p):
+            hv = {t: W.host_values(cfg, r, np.arange(starts[t], starts[t] + numel[t])) for t in members}
+            ins.append(ob.flatten([hv.get(t, np.zeros(0, np.float32)) for t in range(len(numel))], members,
+                                  red.offset, n))
+        want, _ = orc.allreduce(ins, n, W.divisor(cfg))
+        for r in range(p):
+            back = ob.unflatten(want[r], members, red.offset, numel)
+            for t in members:
+                assert_bit_equal(to_host(grads[r][t]), back[t], f"tensor {t} replica {r}")
+    assert D.ddp_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["resnet50", "gpt2_small"])
+def test_model_sized_sync_sampled_parity(name):
+    """Full-size fp32 gradient sets in the bench's launch configuration."""
+    cfg = W.CONFIGS[name]
+    grads, _ = W.make_grads(cfg)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED)
+    torch.cuda.synchronize()
+    _check_sync_sampled(cfg, red, grads, np.random.default_rng(5))
+    # every replica ends identical (the data-parallel invariant), on whole tensors
+    for t in range(len(grads[0])):
+        for r in range(1, cfg["p"]):
+            assert torch.equal(grads[r][t].view(torch.int32), grads[0][t].view(torch.int32))
+    assert D.ddp_device_error() == 0
+
+
+def test_llama_bf16_sync_and_buffer_broadcast_sampled_parity():
+    """1.2B bf16 gradients on 8 replicas (about 39 GB with the buckets), and the
+    per-forward broadcast of 64 fp32 buffers from replica 0."""
+    cfg = W.CONFIGS["llama_1b"]
+    bufs = W.buffer_set(cfg)
+    root_bytes = [b.cpu().numpy().view(np.uint8).copy() for b in bufs[0]]
+    broadcast_buffers(bufs, 0)
+    for r in range(cfg["p"]):
+        for j, b in enumerate(bufs[r]):
+            assert np.array_equal(b.cpu().numpy().view(np.uint8), root_bytes[j])
+    grads, _ = W.make_grads(cfg)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    assert len(red.buckets) == 66
+    red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED)
+    torch.cuda.synchronize()
+    _check_sync_sampled(cfg, red, grads, np.random.default_rng(6), per_bucket=300)
+    assert D.ddp_device_error() == 0
