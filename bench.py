@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="resnet50", choices=sorted(WORKLOAD_TEXT))
-    ap.add_argument("--algo", default="fused", choices=["fused", "ldst", "ring_steps"])
+    ap.add_argument("--algo", default="fused", choices=["fused", "ldst", "tma", "ring_steps"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--sweep", action="store_true", help="message-size / rank-count sweep, one line per point")
@@ -183,7 +183,8 @@ def cores_used() -> int:
 
 def algo_code(name):
     import ring_all_reduce_ddp_gb300 as D
-    return {"fused": D.DDP_ALGO_FUSED, "ldst": D.DDP_ALGO_FUSED_LDST, "ring_steps": D.DDP_ALGO_RING_STEPS}[name]
+    return {"fused": D.DDP_ALGO_FUSED, "ldst": D.DDP_ALGO_FUSED_LDST, "tma": D.DDP_ALGO_FUSED_TMA,
+            "ring_steps": D.DDP_ALGO_RING_STEPS}[name]
 
 
 def kernel_sha() -> str:

@@ -59,9 +59,13 @@ typedef enum {
 typedef enum { DDP_FLOAT32 = 0, DDP_BFLOAT16 = 1 } ddp_dtype;
 
 typedef enum {
-  DDP_ALGO_FUSED = 0,       /* one pass: read p contributions, write p results    */
-  DDP_ALGO_RING_STEPS = 1,  /* the literal schedule: one launch per ring step      */
-  DDP_ALGO_FUSED_LDST = 2   /* one pass, register-only variant (no shared memory)  */
+  DDP_ALGO_FUSED = 0,       /* one pass: read p contributions, write p results; the
+                               library picks its fastest one-pass kernel             */
+  DDP_ALGO_RING_STEPS = 1,  /* the literal schedule: one launch per ring step         */
+  DDP_ALGO_FUSED_LDST = 2,  /* one pass through registers (128-bit loads and stores) */
+  DDP_ALGO_FUSED_TMA = 3    /* one pass staged through shared memory by bulk
+                               asynchronous copies (falls back to the register path
+                               when p > 64 or the replicas' alignments differ)      */
 } ddp_algo;
 
 typedef enum {
@@ -146,8 +150,9 @@ ddp_status ddp_bucket_unflatten(int32_t p, int32_t k, const void* const* bucket,
  * accumulates chunk c, starting at rank c. bf16 inputs are widened to fp32,
  * and y is rounded to bf16 (nearest even). divisor: 1 (sum), p (average) or a
  * token count; must be finite and non-zero.
- * algo DDP_ALGO_FUSED / DDP_ALGO_FUSED_LDST: one pass; RING_STEPS: 2(p-1)
- * launches of the literal schedule (bf16 keeps fp32 partials in a temporary). */
+ * algo DDP_ALGO_FUSED / _FUSED_LDST / _FUSED_TMA: one pass, the same bits;
+ * RING_STEPS: 2(p-1) launches of the literal schedule (bf16 keeps fp32
+ * partials in a stream-ordered temporary). */
 ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype,
                          float divisor, ddp_algo algo, cudaStream_t stream);
 

@@ -267,7 +267,8 @@ ddp_status run_plan_once(Plan& pl, cudaStream_t s) {
 }
 
 ddp_status check_algo(int algo) {
-  DDP_CHECK(algo == DDP_ALGO_FUSED || algo == DDP_ALGO_RING_STEPS || algo == DDP_ALGO_FUSED_LDST,
+  DDP_CHECK(algo == DDP_ALGO_FUSED || algo == DDP_ALGO_RING_STEPS || algo == DDP_ALGO_FUSED_LDST ||
+                algo == DDP_ALGO_FUSED_TMA,
             DDP_ERR_ARG, "unknown algo");
   return DDP_OK;
 }
@@ -456,7 +457,7 @@ ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtyp
     return run_plan_once(pl, stream);
   }
   return run_fused(const_cast<const void* const*>(bufs), bufs, p, n, dtype, divisor, false, 0,
-                   algo == DDP_ALGO_FUSED, stream);
+                   algo == DDP_ALGO_FUSED_TMA, stream);
 }
 
 ddp_status ddp_reduce_scatter(const void* const* in, void* const* out, int32_t p, int64_t n, ddp_dtype dtype,
@@ -489,7 +490,7 @@ ddp_status ddp_reduce_scatter(const void* const* in, void* const* out, int32_t p
     return run_plan_once(pl, stream);
   }
   return run_fused(in, out, p, n, dtype, divisor, true, own == DDP_OWN_RANK ? 1 : 0,
-                   algo == DDP_ALGO_FUSED, stream);
+                   algo == DDP_ALGO_FUSED_TMA, stream);
 }
 
 ddp_status ddp_allgather(const void* const* in, void* const* out, int32_t p, int64_t m, ddp_dtype dtype,

@@ -78,6 +78,24 @@ struct FusedArgs {
   int same_align;    // every src / dst base has the same address mod 16
 };
 
+// Fused reduction staged through shared memory by bulk (TMA) copies. Chunk c's
+// 16-byte-aligned body [body_lo[c], body_lo[c] + body_len[c]) is cut into tiles
+// of tile_elems; tile0 is the prefix of tiles over chunks. The few elements of
+// a chunk outside its body take the scalar path.
+constexpr int kMaxStagedP = 64;
+struct StagedArgs {
+  void* rep[kMaxStagedP];      // the p input replicas (the all-reduce's outputs too)
+  void* out[kMaxStagedP];      // reduce-scatter: out[rank]
+  int64_t body_lo[kMaxStagedP];
+  int64_t body_len[kMaxStagedP];
+  int32_t tile0[kMaxStagedP + 1];
+  int64_t n, cs;
+  float divisor;
+  int p, scatter, shift;
+  int stages, tile_elems;
+  int64_t timeout_ns;          // bound of every wait on a bulk copy
+};
+
 // Literal reduce-scatter step. x[r]: replica r's input (const except in the
 // fp32 in-place all-reduce); w: fp32 partials [2][p][cs]; out[d]: where the
 // last step writes (at chunk-relative index if out_rel, else at i).

@@ -12,7 +12,7 @@ from tests.helpers import assert_bf16_close, assert_bit_equal, make_replicas, to
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-ALGOS = [D.DDP_ALGO_FUSED, D.DDP_ALGO_FUSED_LDST, D.DDP_ALGO_RING_STEPS]
+ALGOS = [D.DDP_ALGO_FUSED, D.DDP_ALGO_FUSED_LDST, D.DDP_ALGO_FUSED_TMA, D.DDP_ALGO_RING_STEPS]
 DT = {"f32": D.DDP_FLOAT32, "bf16": D.DDP_BFLOAT16}
 
 # (p, n): several tiles and chunks, ragged tails, n < p, n not divisible by p
