@@ -202,6 +202,28 @@ ddp_status ddp_broadcast_coalesced(int32_t p, int32_t k, void* const* tensors,
                                    int64_t bucket_cap_bytes, ddp_algo algo,
                                    cudaStream_t stream);
 
+/* Reduce-scatter that allocates nothing. No counterpart in the paper: it exists
+ * for callers that cannot allocate device memory during a call -- for example a
+ * framework whose caching allocator already owns all of the device's memory, or
+ * code that must not risk an allocation failing, or synchronising, in the
+ * middle of a training step.
+ * Same arguments, layout, ownerships, results and errors as ddp_reduce_scatter
+ * with DDP_ALGO_RING_STEPS (the literal p-1 step ring), but the fp32 partials
+ * live in a fixed 8 MiB device array inside the library instead of a
+ * temporary: it calls no cudaMalloc, cudaMallocAsync or cudaFree.
+ *   Limit: 2 * p * ceil(n/p) * 4 bytes <= 8 MiB (p * ceil(n/p) <= 1,048,576
+ *   elements); larger calls return DDP_ERR_ARG with a message and enqueue
+ *   nothing. p == 1 needs no scratch and has no limit.
+ *   The array is one per device, shared by every call, and keeps the last
+ *   call's contents (no call depends on them). Calls whose work overlaps on the
+ *   GPU (different streams, or threads) race on it: order them on one stream.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture. Every GPU that loads the library holds the
+ *   8 MiB until the process exits. */
+ddp_status ddp_reduce_scatter_noalloc(const void* const* in, void* const* out, int32_t p, int64_t n,
+                                      ddp_dtype dtype, float divisor, ddp_own own, cudaStream_t stream);
+
 /* ------------------------------------------- literal schedule, stepwise */
 
 /* A handle that runs one collective's literal schedule one step at a time, so

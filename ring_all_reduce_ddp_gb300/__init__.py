@@ -46,6 +46,7 @@ _SIGS = {
     "ddp_allreduce": [_P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32, _c_vp],
     "ddp_reduce_scatter": [_P_vp, _P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32, _c_i32, _c_vp],
     "ddp_allgather": [_P_vp, _P_vp, _c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_vp],
+    "ddp_reduce_scatter_noalloc": [_P_vp, _P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32, _c_vp],
     "ddp_broadcast": [_P_vp, _c_i32, _c_i64, _c_i32, _c_i32, _c_vp],
     "ddp_broadcast_coalesced": [_c_i32, _c_i32, _P_vp, _P_i64, _c_i32, _c_i64, _c_i32, _c_vp],
     "ddp_ring_create": [ctypes.POINTER(_c_vp), _c_i32, _P_vp, _P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32,
@@ -193,6 +194,14 @@ def ddp_reduce_scatter(ins, outs, n: int, dtype=DDP_FLOAT32, divisor: float = 1.
                        algo: int = DDP_ALGO_FUSED, stream=None):
     _check(lib().ddp_reduce_scatter(_ptrs(ins), _ptrs(outs), len(ins), int(n), _dtype(dtype), float(divisor),
                                     own, algo, _stream(stream)))
+
+
+def ddp_reduce_scatter_noalloc(ins, outs, n: int, dtype=DDP_FLOAT32, divisor: float = 1.0,
+                               own: int = DDP_OWN_RANK, stream=None):
+    """The literal ring reduce-scatter with its partials in the library's fixed
+    scratch array: for callers that cannot allocate device memory mid-step."""
+    _check(lib().ddp_reduce_scatter_noalloc(_ptrs(ins), _ptrs(outs), len(ins), int(n), _dtype(dtype),
+                                            float(divisor), own, _stream(stream)))
 
 
 def ddp_allgather(ins, outs, m: int, dtype=DDP_FLOAT32, own: int = DDP_OWN_RANK, algo: int = DDP_ALGO_FUSED,
