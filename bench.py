@@ -46,8 +46,9 @@ WORKLOAD_TEXT = {
     "tiny": "ten odd-sized fp32 tensors (277,421 elements), p=4, 16 KiB / 256 KiB buckets, average by 1/4",
 }
 
-# DRAM traffic of the fused all-reduce kernel from an ncu capture (bytes per
-# launch per algorithmic byte), valid only while the kernel source is unchanged.
+# DRAM traffic of the dominant kernel (the in-place bucket all-reduce) from an
+# ncu capture, as bytes per algorithmic byte; valid only while the kernel
+# source it was taken on is unchanged (checked by hash).
 NCU_TRAFFIC = {"kernel_sha256": None, "dram_bytes_per_algorithmic_byte": None}
 
 
@@ -59,6 +60,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="resnet50", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--algo", default="fused", choices=["fused", "ldst", "tma", "ring_steps"])
+    ap.add_argument("--mode", default="in_place", choices=["in_place", "flatten"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--sweep", action="store_true", help="message-size / rank-count sweep, one line per point")
@@ -78,14 +80,15 @@ class Ranks:
         if self.world > 1:
             import torch
             import torch.distributed as dist
-            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            backend = os.environ.get("DDP_BENCH_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
             dist.init_process_group(backend)
+            self.backend = backend
             self.dist = dist
 
     def barrier(self):
         if self.dist is not None:
             import torch
-            if torch.cuda.is_available():
+            if self.backend == "nccl":
                 self.dist.barrier(device_ids=[self.local])
             else:
                 self.dist.barrier()
@@ -94,7 +97,7 @@ class Ranks:
         if self.dist is None:
             return x
         import torch
-        dev = f"cuda:{self.local}" if torch.cuda.is_available() else "cpu"
+        dev = f"cuda:{self.local}" if self.backend == "nccl" else "cpu"
         t = torch.tensor([x], dtype=torch.float64, device=dev)
         self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
         return float(t.item())
@@ -190,7 +193,7 @@ def algo_code(name):
 def kernel_sha() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("k_reduce.cu", "common.cuh"):
+    for f in ("k_bucket.cu", "common.cuh"):
         with open(os.path.join(ROOT, "ring_all_reduce_ddp_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -243,7 +246,7 @@ def run_ours(args, ranks: Ranks):
 
     import ring_all_reduce_ddp_gb300 as D
     from ring_all_reduce_ddp_gb300 import build as B
-    from ring_all_reduce_ddp_gb300.reducer import Reducer, broadcast_buffers
+    from ring_all_reduce_ddp_gb300.reducer import BufferSync, Reducer
     from synth import workloads as W
 
     B.build_library()
@@ -252,22 +255,34 @@ def run_ours(args, ranks: Ranks):
     cfg = W.CONFIGS[args.config]
     p = cfg["p"]
     algo = algo_code(args.algo)
+    mode = D.DDP_SYNC_IN_PLACE if args.mode == "in_place" else D.DDP_SYNC_FLATTEN
+    if args.algo == "ring_steps":
+        mode = D.DDP_SYNC_FLATTEN
     grads, arenas = W.make_grads(cfg, f"cuda:{dev}")
     bufs = W.buffer_set(cfg, f"cuda:{dev}") if cfg.get("buffers") else None
     red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    bsync = BufferSync(bufs, 0) if bufs else None
     divisor = W.divisor(cfg)
     stream = torch.cuda.current_stream()
     bc_algo = D.DDP_ALGO_RING_STEPS if args.algo == "ring_steps" else D.DDP_ALGO_FUSED
-    buf_bytes = sum(t.numel() * t.element_size() for t in bufs[0]) if bufs else 0
+    buf_bytes = sum(bsync.nbytes) if bsync else 0
+    esz = W.esize(cfg)
 
-    def step(events=None):
-        if not red.assign():
+    def step(events=None, m=mode):
+        if not red.assign():  # a1: bucket assignment (host)
             raise RuntimeError("bucket assignment changed")
-        if bufs:
-            broadcast_buffers(bufs, 0, 0, bc_algo, stream)
-        red.sync_gradients(divisor, algo, stream=stream, allreduce_events=events)
+        if bsync:             # a9: the forward's buffer broadcast
+            bsync(bc_algo, stream)
+        if events is not None:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        red.sync_gradients(divisor, algo, m, 1.0, stream)  # a2-a8
+        if events is not None:
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(stream)
+            events.append((e0, e1))
 
-    ab = red.algorithmic_bytes()
+    ab = red.algorithmic_bytes(mode)
     step_bytes = ab["total"] + p * buf_bytes
     for _ in range(max(args.warmup, 0)):
         step()
@@ -278,13 +293,13 @@ def run_ours(args, ranks: Ranks):
     sampler.start()
     time.sleep(0.3)
     launches0 = D.ddp_kernel_launches()
-    ar_events: list = []
+    sync_events: list = []
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     ranks.barrier()
     e0.record(stream)
     for _ in range(args.steps):
-        step(ar_events)
+        step(sync_events)
     e1.record(stream)
     torch.cuda.synchronize()
     ranks.barrier()
@@ -295,69 +310,91 @@ def run_ours(args, ranks: Ranks):
     ms_per_step = ms_max / args.steps
     value = step_bytes * args.steps * ranks.world / (ms_max / 1e3) / 1e9
 
-    # dominant kernel: the fused all-reduce, timed per launch with events on its stream
-    ar_ms = [a.elapsed_time(b) for a, b in ar_events]
-    ar_bytes_per_launch = [2 * p * n * W.esize(cfg) for n in red.bucket_numel] * args.steps
-    achieved = sum(ar_bytes_per_launch) / (sum(ar_ms) / 1e3) / 1e9
+    # Dominant kernel: the bucket all-reduce (in place: one launch per bucket, back to back).
+    # Its duration is taken from events around each step's launches of it, so the
+    # few-microsecond gaps between consecutive launches count against it.
+    sync_ms = [a.elapsed_time(b) for a, b in sync_events]
+    nb = len(red.buckets)
+    achieved = ab["allreduce"] * len(sync_ms) / (sum(sync_ms) / 1e3) / 1e9
     peak, peak_kind = peak_hbm()
     traffic = None
     if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]:
-        traffic = int(NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * (ab["allreduce"] / len(red.buckets)))
-    bucket_mb = [round(n * W.esize(cfg) / 2 ** 20, 2) for n in red.bucket_numel]
+        traffic = int(NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * (ab["allreduce"] / nb))
+    bucket_mb = [round(n * esz / 2 ** 20, 2) for n in red.bucket_numel]
+    kernel_name = ("k_bucket_allreduce (flatten + ring-order all-reduce + unflatten in one pass)"
+                   if mode == D.DDP_SYNC_IN_PLACE else "flatten, fused all-reduce, unflatten (three kernels)")
 
-    # end to end through the public API: pinned host gradients in, synchronised gradients out
-    if True:
-        host_in = [a.detach().to("cpu").pin_memory() for a in arenas]
-        host_out = [torch.empty_like(h).pin_memory() for h in host_in]
-        k_e2e = args.steps
-        for _ in range(min(3, max(args.warmup, 1))):
-            for a, h in zip(arenas, host_in):
-                a.copy_(h, non_blocking=True)
-            step()
-            for a, h in zip(arenas, host_out):
-                h.copy_(a, non_blocking=True)
+    # End to end through the public API: every replica's gradients in from pinned
+    # host memory, one step, the synchronised gradients out, every step.
+    host_in = [a.detach().to("cpu").pin_memory() for a in arenas]
+    host_out = [torch.empty_like(h).pin_memory() for h in host_in]
+
+    def e2e_step():
+        for a, h in zip(arenas, host_in):
+            a.copy_(h, non_blocking=True)
+        step()
+        for a, h in zip(arenas, host_out):
+            h.copy_(a, non_blocking=True)
+
+    for _ in range(min(3, max(args.warmup, 1))):
+        e2e_step()
+    torch.cuda.synchronize()
+    ranks.barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    e2e_ms = ranks.max(f0.elapsed_time(f1))
+    io = sum(a.numel() * a.element_size() for a in arenas)
+    e2e = {"value": round(step_bytes * args.steps * ranks.world / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+           "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "ms_per_step": round(e2e_ms / args.steps, 4)}
+
+    # the three-kernel form of the same step, for comparison (not the headline)
+    other = None
+    if mode == D.DDP_SYNC_IN_PLACE:
+        k2 = max(10, args.steps // 5)
+        for _ in range(3):
+            step(None, D.DDP_SYNC_FLATTEN)
         torch.cuda.synchronize()
-        ranks.barrier()
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(k_e2e):
-            for a, h in zip(arenas, host_in):
-                a.copy_(h, non_blocking=True)
-            step()
-            for a, h in zip(arenas, host_out):
-                h.copy_(a, non_blocking=True)
-        f1.record(stream)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(k2):
+            step(None, D.DDP_SYNC_FLATTEN)
+        g1.record(stream)
         torch.cuda.synchronize()
-        ranks.barrier()
-        e2e_ms = ranks.max(f0.elapsed_time(f1))
-        io = sum(a.numel() * a.element_size() for a in arenas)
-        e2e = {"value": round(step_bytes * k_e2e * ranks.world / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
-               "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "ms_per_step": round(e2e_ms / k_e2e, 4)}
+        fl = red.algorithmic_bytes(D.DDP_SYNC_FLATTEN)["total"] + p * buf_bytes
+        ms2 = g0.elapsed_time(g1) / k2
+        other = {"mode": "flatten + all-reduce + unflatten", "ms_per_step": round(ms2, 5),
+                 "gbs": round(fl / (ms2 / 1e3) / 1e9, 1), "steps": k2}
 
     cpu = None
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
-        nb, secs, desc = oracle_sync_sample(cfg, args.cpu_budget_s)
-        cpu = {"value": round(nb / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
+        nbytes, secs, desc = oracle_sync_sample(cfg, args.cpu_budget_s)
+        cpu = {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
                "host_cores_available": cores_used()}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ranks.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg["dtype"], "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.config], "p": p, "buckets": len(red.buckets),
-                   "bucket_mb": bucket_mb, "algo": args.algo, "divisor": divisor,
-                   "l2": "inputs larger than L2: %.2f GB of gradients + %.2f GB of buckets per step" %
-                         (sum(a.numel() * a.element_size() for a in arenas) / 1e9, ab["allreduce"] / 2 / 1e9),
+        "config": {"workload": WORKLOAD_TEXT[args.config], "p": p, "buckets": nb, "bucket_mb": bucket_mb,
+                   "algo": args.algo, "sync": "in_place" if mode == D.DDP_SYNC_IN_PLACE else "flatten",
+                   "divisor": divisor,
+                   "l2": "inputs larger than L2: %.2f GB of gradients per step" %
+                         (sum(a.numel() * a.element_size() for a in arenas) / 1e9),
                    "parallelism": f"replicas only: {ranks.world} independent GPU(s)"},
-        "roofline": {"bound": "hbm", "kernel": "fused ring-order all-reduce", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic,
-                     "algorithmic_bytes_per_launch": int(ab["allreduce"] / len(red.buckets)),
-                     "avg_launch_us": round(1e3 * statistics.mean(ar_ms), 2)},
+                     "traffic": traffic, "algorithmic_bytes_per_launch": int(ab["allreduce"] / nb),
+                     "avg_launch_us": round(1e3 * statistics.mean(sync_ms) / nb, 2)},
         "allreduce_gbs": round(achieved, 1),
-        "buckets_per_s": round(len(red.buckets) * args.steps * ranks.world / (ms_max / 1e3), 1),
-        "busbw_gbs": round(sum(n * W.esize(cfg) for n in red.bucket_numel) / (sum(ar_ms) / args.steps / 1e3)
-                           / 1e9 * 2 * (p - 1) / p, 1),
+        "buckets_per_s": round(nb * args.steps * ranks.world / (ms_max / 1e3), 1),
+        "busbw_gbs": round(sum(n * esz for n in red.bucket_numel) / (statistics.mean(sync_ms) / 1e3) / 1e9
+                           * 2 * (p - 1) / p, 1),
+        "flatten_form": other,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
     if ranks.rank == 0:

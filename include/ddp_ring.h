@@ -80,6 +80,11 @@ typedef enum {
 } ddp_border;
 
 typedef enum {
+  DDP_SYNC_FLATTEN = 0,  /* per bucket: flatten, all-reduce the flat bucket; then unflatten */
+  DDP_SYNC_IN_PLACE = 1  /* per bucket: one pass over the gradients themselves            */
+} ddp_sync_mode;
+
+typedef enum {
   DDP_OP_ALLREDUCE = 0,
   DDP_OP_REDUCE_SCATTER = 1,
   DDP_OP_ALLGATHER = 2,
@@ -201,6 +206,47 @@ ddp_status ddp_broadcast_coalesced(int32_t p, int32_t k, void* const* tensors,
                                    const int64_t* nbytes, int32_t root,
                                    int64_t bucket_cap_bytes, ddp_algo algo,
                                    cudaStream_t stream);
+
+/* All-reduce of one bucket straight on the gradients: the result of
+ * ddp_bucket_flatten, ddp_allreduce(DDP_ALGO_FUSED) on the flat bucket and
+ * ddp_bucket_unflatten, bit for bit, in one pass that reads every replica's
+ * gradients once and writes them once (no flat buffer). [DDP] Part 2,
+ * mark_variable_ready / all_reduce_bucket / finalize_backward; [COLL] "Ring
+ * allreduce in two passes". Element e of tensor j sits at bucket position
+ * offset[j] + e, in chunk (offset[j] + e) / ceil(n/p) with n = max(offset[j] +
+ * numel[j]); it is summed in that chunk's ring order and divided by divisor.
+ *   grads[p*k]: grads[r*k + j] is replica r's tensor j (in place);
+ *   numel[k], offset[k]: as from ddp_bucket_assign. Tensors must not overlap. */
+ddp_status ddp_bucket_allreduce(int32_t p, int32_t k, void* const* grads, const int64_t* numel,
+                                const int64_t* offset, ddp_dtype dtype, float divisor,
+                                cudaStream_t stream);
+
+/* ------------------------------------------------------------- reducer */
+
+/* A Reducer for p replicas: the gradient synchronisation of [DDP] Part 2 in
+ * one call. ddp_reducer_create assigns the buckets (ddp_bucket_assign with
+ * the given caps and order), allocates every replica's flat buckets (handle
+ * workspace, freed by ddp_reducer_destroy) and plans every launch once.
+ *   grads[p*k]: grads[r*k + t] is replica r's gradient t (registration order),
+ *   numel[k] elements each; kept (not copied) until destroy.
+ * ddp_reducer_sync enqueues, on `stream`, one synchronisation:
+ *   DDP_SYNC_FLATTEN: for every bucket in order, ddp_bucket_flatten (with
+ *     predivide) then ddp_allreduce with `algo`; then ddp_bucket_unflatten of
+ *     every bucket ([DDP] "Step 3: finalize_backward").
+ *   DDP_SYNC_IN_PLACE: for every bucket in order, ddp_bucket_allreduce
+ *     (fused algos only; predivide must be 1).
+ * Both give the same bits. */
+typedef struct ddp_reducer ddp_reducer;
+ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* const* grads,
+                              const int64_t* numel, ddp_dtype dtype, int64_t first_bucket_cap_bytes,
+                              int64_t bucket_cap_bytes, ddp_border order);
+/* Number of buckets; -1 for a null handle. */
+int32_t ddp_reducer_num_buckets(const ddp_reducer* handle);
+/* Bucket b's element count and (if flat != NULL) its p flat buffers. */
+ddp_status ddp_reducer_bucket(const ddp_reducer* handle, int32_t b, int64_t* numel, void** flat);
+ddp_status ddp_reducer_sync(ddp_reducer* handle, float divisor, float predivide, ddp_algo algo,
+                            ddp_sync_mode mode, cudaStream_t stream);
+ddp_status ddp_reducer_destroy(ddp_reducer* handle);
 
 /* Reduce-scatter that allocates nothing. No counterpart in the paper: it exists
  * for callers that cannot allocate device memory during a call -- for example a

@@ -29,6 +29,8 @@ DDP_ALGO_FUSED, DDP_ALGO_RING_STEPS, DDP_ALGO_FUSED_LDST, DDP_ALGO_FUSED_TMA = 0
 DDP_OWN_RANK, DDP_OWN_RING = 0, 1
 # ddp_border
 DDP_ORDER_REVERSED, DDP_ORDER_REGISTRATION = 0, 1
+# ddp_sync_mode
+DDP_SYNC_FLATTEN, DDP_SYNC_IN_PLACE = 0, 1
 # ddp_op
 DDP_OP_ALLREDUCE, DDP_OP_REDUCE_SCATTER, DDP_OP_ALLGATHER, DDP_OP_BROADCAST = 0, 1, 2, 3
 DDP_MAX_P = 256
@@ -46,6 +48,12 @@ _SIGS = {
     "ddp_allreduce": [_P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32, _c_vp],
     "ddp_reduce_scatter": [_P_vp, _P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32, _c_i32, _c_vp],
     "ddp_allgather": [_P_vp, _P_vp, _c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_vp],
+    "ddp_bucket_allreduce": [_c_i32, _c_i32, _P_vp, _P_i64, _P_i64, _c_i32, _c_f32, _c_vp],
+    "ddp_reducer_create": [ctypes.POINTER(_c_vp), _c_i32, _c_i32, _P_vp, _P_i64, _c_i32, _c_i64, _c_i64, _c_i32],
+    "ddp_reducer_num_buckets": [_c_vp],
+    "ddp_reducer_bucket": [_c_vp, _c_i32, _P_i64, _P_vp],
+    "ddp_reducer_sync": [_c_vp, _c_f32, _c_f32, _c_i32, _c_i32, _c_vp],
+    "ddp_reducer_destroy": [_c_vp],
     "ddp_reduce_scatter_noalloc": [_P_vp, _P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32, _c_vp],
     "ddp_broadcast": [_P_vp, _c_i32, _c_i64, _c_i32, _c_i32, _c_vp],
     "ddp_broadcast_coalesced": [_c_i32, _c_i32, _P_vp, _P_i64, _c_i32, _c_i64, _c_i32, _c_vp],
@@ -63,7 +71,7 @@ _SIGS = {
     "ddp_last_error": [],
     "ddp_status_string": [_c_i32],
 }
-_RESTYPES = {"ddp_ring_num_steps": _c_i32, "ddp_ring_steps_done": _c_i32, "ddp_kernel_launches": _c_i64,
+_RESTYPES = {"ddp_reducer_num_buckets": _c_i32, "ddp_ring_num_steps": _c_i32, "ddp_ring_steps_done": _c_i32, "ddp_kernel_launches": _c_i64,
              "ddp_last_error": ctypes.c_char_p, "ddp_status_string": ctypes.c_char_p}
 
 _lib = None
@@ -112,6 +120,9 @@ def _ptr(x) -> int:
 
 
 def _ptrs(seq):
+    """A ctypes array of pointers (passed through if it already is one)."""
+    if isinstance(seq, ctypes.Array):
+        return seq
     arr = (ctypes.c_void_p * max(1, len(seq)))()
     for i, x in enumerate(seq):
         arr[i] = _ptr(x)
@@ -119,6 +130,8 @@ def _ptrs(seq):
 
 
 def _i64s(seq):
+    if isinstance(seq, ctypes.Array):
+        return seq
     arr = (ctypes.c_int64 * max(1, len(seq)))()
     for i, x in enumerate(seq):
         arr[i] = int(x)
@@ -215,10 +228,13 @@ def ddp_broadcast(bufs, nbytes: int, root: int = 0, algo: int = DDP_ALGO_FUSED, 
 
 
 def ddp_broadcast_coalesced(tensors, nbytes, root: int = 0, bucket_cap_bytes: int = 0,
-                            algo: int = DDP_ALGO_FUSED, stream=None):
-    """tensors: p lists of k tensors (or a flat replica-major list of p*k pointers)."""
+                            algo: int = DDP_ALGO_FUSED, stream=None, p: int | None = None):
+    """tensors: p lists of k tensors, a flat replica-major list of p*k pointers,
+    or (with p given) a prebuilt ctypes pointer array."""
     k = len(nbytes)
-    if tensors and isinstance(tensors[0], (list, tuple)):
+    if isinstance(tensors, ctypes.Array):
+        flat = tensors
+    elif tensors and isinstance(tensors[0], (list, tuple)):
         p = len(tensors)
         flat = [t for row in tensors for t in row]
     else:
@@ -226,6 +242,62 @@ def ddp_broadcast_coalesced(tensors, nbytes, root: int = 0, bucket_cap_bytes: in
         flat = list(tensors)
     _check(lib().ddp_broadcast_coalesced(p, k, _ptrs(flat), _i64s(nbytes), int(root), int(bucket_cap_bytes),
                                          algo, _stream(stream)))
+
+
+def ddp_bucket_allreduce(grads, numel, offset, dtype=DDP_FLOAT32, divisor: float = 1.0, stream=None):
+    """One bucket's all-reduce straight on the gradients. grads: p lists of the
+    bucket's k tensors (walk order), or a flat replica-major list of p*k pointers."""
+    k = len(numel)
+    if grads and isinstance(grads[0], (list, tuple)):
+        p = len(grads)
+        flat = [g for row in grads for g in row]
+    else:
+        p = len(grads) // max(1, k)
+        flat = list(grads)
+    _check(lib().ddp_bucket_allreduce(p, k, _ptrs(flat), _i64s(numel), _i64s(offset), _dtype(dtype),
+                                      float(divisor), _stream(stream)))
+
+
+class DDPReducer:
+    """ddp_reducer_create / sync / destroy: a whole gradient synchronisation per call."""
+
+    def __init__(self, grads, first_bucket_cap_bytes: int = 1 << 20, bucket_cap_bytes: int = 25 << 20,
+                 order: int = DDP_ORDER_REVERSED):
+        self.p = len(grads)
+        self.k = len(grads[0])
+        self.dtype = _dtype(grads[0][0].dtype)
+        numel = [g.numel() for g in grads[0]]
+        h = ctypes.c_void_p(0)
+        self._grads = _ptrs([g for row in grads for g in row])
+        _check(lib().ddp_reducer_create(ctypes.byref(h), self.p, self.k, self._grads, _i64s(numel), self.dtype,
+                                        int(first_bucket_cap_bytes), int(bucket_cap_bytes), int(order)))
+        self.h = h
+
+    def num_buckets(self) -> int:
+        return lib().ddp_reducer_num_buckets(self.h)
+
+    def bucket(self, b: int):
+        """(element count, [p flat-buffer device pointers]) of bucket b."""
+        n = ctypes.c_int64(0)
+        flat = (ctypes.c_void_p * self.p)()
+        _check(lib().ddp_reducer_bucket(self.h, int(b), ctypes.byref(n), flat))
+        return n.value, [flat[r] for r in range(self.p)]
+
+    def sync(self, divisor: float, algo: int = DDP_ALGO_FUSED, mode: int = DDP_SYNC_IN_PLACE,
+             predivide: float = 1.0, stream=None):
+        _check(lib().ddp_reducer_sync(self.h, float(divisor), float(predivide), int(algo), int(mode),
+                                      _stream(stream)))
+
+    def destroy(self):
+        if self.h:
+            _check(lib().ddp_reducer_destroy(self.h))
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
 
 
 # ------------------------------------------------------- literal schedule

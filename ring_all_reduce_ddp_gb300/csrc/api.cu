@@ -352,6 +352,66 @@ ddp_status check_bucket_layout(int32_t p, int32_t k, const void* const* grads, c
   return DDP_OK;
 }
 
+
+// Pieces of one bucket for the in-place kernel: every tensor cut at chunk
+// boundaries, so each piece has one summation origin. Launches hold at most
+// kBucketPieces pieces and kBucketPtrs replica pointers; a longer bucket goes
+// out in several launches (pieces are independent).
+ddp_status plan_bucket_launches(int32_t p, int32_t k, const void* const* grads, const int64_t* numel,
+                                const int64_t* offset, ddp_dtype dt, float divisor,
+                                std::vector<BucketArgs>& out) {
+  out.clear();
+  int64_t n = 0;
+  for (int32_t j = 0; j < k; ++j) n = std::max(n, offset[j] + numel[j]);
+  if (n == 0) return DDP_OK;
+  const int64_t cs = chunk_size(n, p);
+  const int64_t tile = kBucketTileBytes / esize(dt);
+  const int slots_per_launch = kBucketPtrs / p;
+  DDP_CHECK(slots_per_launch >= 1, DDP_ERR_ARG, "too many replicas for the in-place bucket kernel");
+  BucketArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.p = p;
+  a.divisor = divisor;
+  int nslots = 0;
+  auto flush = [&]() {
+    if (a.npieces > 0) out.push_back(a);
+    std::memset(&a, 0, sizeof(a));
+    a.p = p;
+    a.divisor = divisor;
+    nslots = 0;
+  };
+  for (int32_t j = 0; j < k; ++j) {
+    if (numel[j] == 0) continue;
+    const int64_t lo = offset[j], hi = offset[j] + numel[j];
+    const int64_t c0 = lo / cs, c1 = (hi - 1) / cs;
+    if (nslots == slots_per_launch || a.npieces + (c1 - c0 + 1) > kBucketPieces) flush();
+    DDP_CHECK(c1 - c0 + 1 <= kBucketPieces, DDP_ERR_ARG, "a tensor spans too many chunks");
+    const int slot = nslots++;
+    for (int r = 0; r < p; ++r) a.ptr[slot * p + r] = const_cast<void*>(grads[static_cast<int64_t>(r) * k + j]);
+    for (int64_t c = c0; c <= c1; ++c) {
+      const int64_t plo = std::max(lo, c * cs), phi = std::min(hi, (c + 1) * cs);
+      const int i = a.npieces++;
+      a.start[i] = plo - lo;
+      a.len[i] = phi - plo;
+      a.slot[i] = slot;
+      a.origin[i] = static_cast<int32_t>(c);
+      const int64_t tiles = (phi - plo + tile - 1) / tile;
+      DDP_CHECK(static_cast<int64_t>(a.tile0[i]) + tiles <= 0x7FFFFFFF, DDP_ERR_ARG, "bucket too large");
+      a.tile0[i + 1] = a.tile0[i] + static_cast<int32_t>(tiles);
+    }
+  }
+  flush();
+  return DDP_OK;
+}
+
+ddp_status run_bucket_launches(std::vector<BucketArgs>& launches, ddp_dtype dt, float divisor, cudaStream_t s) {
+  for (BucketArgs& a : launches) {
+    a.divisor = divisor;
+    DDP_CUDA(launch_bucket_allreduce(a, dt, s), "bucket all-reduce launch");
+  }
+  return DDP_OK;
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -676,6 +736,201 @@ ddp_status ddp_broadcast_coalesced(int32_t p, int32_t k, void* const* tensors, c
   const cudaError_t e = cudaFreeAsync(ws, stream);
   if (rc == DDP_OK && e != cudaSuccess) return cuda_fail(e, "broadcast workspace release");
   return rc;
+}
+
+
+ddp_status ddp_bucket_allreduce(int32_t p, int32_t k, void* const* grads, const int64_t* numel,
+                                const int64_t* offset, ddp_dtype dtype, float divisor, cudaStream_t stream) {
+  DDP_TRY(check_bucket_args(p, k, numel, offset, dtype));
+  DDP_TRY(check_divisor(divisor));
+  const int es = esize(dtype);
+  DDP_CHECK(grads != nullptr || k == 0, DDP_ERR_ARG, "grads array is null");
+  std::vector<std::pair<uintptr_t, uintptr_t>> slots, ranges;
+  for (int32_t j = 0; j < k; ++j)
+    slots.push_back({static_cast<uintptr_t>(offset[j]), static_cast<uintptr_t>(offset[j] + numel[j])});
+  DDP_CHECK(disjoint(slots), DDP_ERR_ARG, "bucket slots of different tensors overlap");
+  for (int32_t r = 0; r < p; ++r)
+    for (int32_t j = 0; j < k; ++j) {
+      if (numel[j] == 0) continue;
+      const void* g = grads[static_cast<int64_t>(r) * k + j];
+      DDP_CHECK(g != nullptr, DDP_ERR_ARG, "grads[" + std::to_string(r * k + j) + "] is null");
+      ranges.push_back(range_of(g, numel[j] * es));
+    }
+  DDP_CHECK(disjoint(ranges), DDP_ERR_ARG, "gradient tensors overlap");
+  std::vector<BucketArgs> launches;
+  DDP_TRY(plan_bucket_launches(p, k, const_cast<const void* const*>(grads), numel, offset, dtype, divisor, launches));
+  return run_bucket_launches(launches, dtype, divisor, stream);
+}
+
+// ------------------------------------------------------------- reducer
+struct ddp_reducer {
+  int32_t p = 0, k = 0;
+  ddp_dtype dt = DDP_FLOAT32;
+  std::vector<void*> grads;  // [p * k]
+  std::vector<int64_t> numel;
+  struct Bucket {
+    std::vector<int32_t> members;
+    std::vector<int64_t> numel, offset;  // per member
+    int64_t n = 0;
+    std::vector<void*> flat;             // [p]
+    std::vector<const void*> grads;      // [p * members], replica-major
+    std::vector<BucketArgs> in_place;    // prebuilt launches
+  };
+  std::vector<Bucket> buckets;
+  std::vector<void*> arenas;  // one flat-bucket arena per replica
+  float* ws = nullptr;        // fp32 partials for the literal bf16 schedule
+  int64_t ws_elems = 0;
+};
+
+ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* const* grads,
+                              const int64_t* numel, ddp_dtype dtype, int64_t first_bucket_cap_bytes,
+                              int64_t bucket_cap_bytes, ddp_border order) {
+  DDP_CHECK(handle != nullptr, DDP_ERR_ARG, "handle pointer is null");
+  *handle = nullptr;
+  DDP_TRY(check_common(p, 0, dtype));
+  DDP_CHECK(k >= 1 && numel && grads, DDP_ERR_ARG, "need k >= 1 tensors, numel and grads");
+  const int es = esize(dtype);
+  std::vector<int32_t> bucket_of(k), bptr(k + 1), btens(k);
+  std::vector<int64_t> offset(k), bnumel(k);
+  int32_t nb = 0;
+  DDP_TRY(ddp_bucket_assign(k, numel, es, first_bucket_cap_bytes, bucket_cap_bytes, order, &nb, bucket_of.data(),
+                            offset.data(), bptr.data(), btens.data(), bnumel.data()));
+  {
+    std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
+    for (int32_t r = 0; r < p; ++r)
+      for (int32_t t = 0; t < k; ++t) {
+        if (numel[t] == 0) continue;
+        const void* g = grads[static_cast<int64_t>(r) * k + t];
+        DDP_CHECK(g != nullptr, DDP_ERR_ARG, "grads[" + std::to_string(r * k + t) + "] is null");
+        ranges.push_back(range_of(g, numel[t] * es));
+      }
+    DDP_CHECK(disjoint(ranges), DDP_ERR_ARG, "gradient tensors overlap");
+  }
+  ddp_reducer* h = new ddp_reducer();
+  h->p = p; h->k = k; h->dt = dtype;
+  h->grads.assign(grads, grads + static_cast<int64_t>(p) * k);
+  h->numel.assign(numel, numel + k);
+  int64_t arena = 0;
+  std::vector<int64_t> base(nb);
+  for (int32_t b = 0; b < nb; ++b) {
+    base[b] = arena;
+    arena += (bnumel[b] * es + 255) / 256 * 256;
+    h->ws_elems = std::max(h->ws_elems, 2 * static_cast<int64_t>(p) * chunk_size(bnumel[b], p));
+  }
+  auto fail_free = [&](ddp_status st, const std::string& msg) {
+    for (void* a : h->arenas) cudaFree(a);
+    if (h->ws) cudaFree(h->ws);
+    delete h;
+    return fail(st, msg);
+  };
+  for (int32_t r = 0; r < p; ++r) {
+    void* a = nullptr;
+    const cudaError_t e = cudaMalloc(&a, std::max<int64_t>(arena, 256));
+    if (e != cudaSuccess) return fail_free(DDP_ERR_NOMEM, std::string("reducer buckets: ") + cudaGetErrorString(e));
+    h->arenas.push_back(a);
+  }
+  if (dtype == DDP_BFLOAT16 && p > 1 && h->ws_elems > 0) {
+    void* w = nullptr;
+    const cudaError_t e = cudaMalloc(&w, h->ws_elems * sizeof(float));
+    if (e != cudaSuccess) return fail_free(DDP_ERR_NOMEM, std::string("reducer workspace: ") + cudaGetErrorString(e));
+    h->ws = static_cast<float*>(w);
+  }
+  for (int32_t b = 0; b < nb; ++b) {
+    ddp_reducer::Bucket B;
+    B.n = bnumel[b];
+    for (int32_t i = bptr[b]; i < bptr[b + 1]; ++i) {
+      const int32_t t = btens[i];
+      B.members.push_back(t);
+      B.numel.push_back(numel[t]);
+      B.offset.push_back(offset[t]);
+    }
+    const int32_t m = static_cast<int32_t>(B.members.size());
+    for (int32_t r = 0; r < p; ++r) {
+      B.flat.push_back(static_cast<char*>(h->arenas[r]) + base[b]);
+      for (int32_t t : B.members) B.grads.push_back(grads[static_cast<int64_t>(r) * k + t]);
+    }
+    const ddp_status st = plan_bucket_launches(p, m, B.grads.data(), B.numel.data(), B.offset.data(), dtype, 1.0f,
+                                               B.in_place);
+    if (st != DDP_OK) return fail_free(st, t_error);
+    h->buckets.push_back(std::move(B));
+  }
+  *handle = h;
+  return DDP_OK;
+}
+
+int32_t ddp_reducer_num_buckets(const ddp_reducer* h) { return h ? static_cast<int32_t>(h->buckets.size()) : -1; }
+
+ddp_status ddp_reducer_bucket(const ddp_reducer* h, int32_t b, int64_t* numel, void** flat) {
+  DDP_CHECK(h && numel, DDP_ERR_ARG, "null argument");
+  DDP_CHECK(b >= 0 && b < static_cast<int32_t>(h->buckets.size()), DDP_ERR_ARG, "bucket index out of range");
+  *numel = h->buckets[b].n;
+  if (flat)
+    for (int32_t r = 0; r < h->p; ++r) flat[r] = h->buckets[b].flat[r];
+  return DDP_OK;
+}
+
+ddp_status ddp_reducer_sync(ddp_reducer* h, float divisor, float predivide, ddp_algo algo, ddp_sync_mode mode,
+                            cudaStream_t stream) {
+  DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
+  DDP_TRY(check_divisor(divisor));
+  DDP_TRY(check_divisor(predivide));
+  DDP_TRY(check_algo(algo));
+  DDP_CHECK(mode == DDP_SYNC_FLATTEN || mode == DDP_SYNC_IN_PLACE, DDP_ERR_ARG, "unknown sync mode");
+  const int p = h->p;
+  if (mode == DDP_SYNC_IN_PLACE) {
+    DDP_CHECK(algo != DDP_ALGO_RING_STEPS, DDP_ERR_ARG, "the in-place sync is the fused form only");
+    DDP_CHECK(predivide == 1.0f, DDP_ERR_ARG, "the in-place sync has no pre-divide");
+    for (auto& B : h->buckets) DDP_TRY(run_bucket_launches(B.in_place, h->dt, divisor, stream));
+    return DDP_OK;
+  }
+  const int es = esize(h->dt);
+  for (auto& B : h->buckets) {
+    const int32_t m = static_cast<int32_t>(B.members.size());
+    SegBatcher sb(h->dt, predivide, stream);
+    for (int32_t r = 0; r < p; ++r)
+      for (int32_t j = 0; j < m; ++j)
+        DDP_TRY(sb.add(B.grads[static_cast<int64_t>(r) * m + j], static_cast<char*>(B.flat[r]) + B.offset[j] * es,
+                       B.numel[j] * es));
+    DDP_TRY(sb.flush());
+    if (B.n == 0) continue;
+    if (algo == DDP_ALGO_RING_STEPS) {
+      Plan pl;
+      pl.op = DDP_OP_ALLREDUCE; pl.p = p; pl.n = B.n; pl.dt = h->dt; pl.divisor = divisor;
+      pl.in.assign(B.flat.begin(), B.flat.end());
+      pl.init();
+      pl.ws = h->ws;
+      DDP_TRY(pl.run_all(stream));
+    } else {
+      DDP_TRY(run_fused(const_cast<const void* const*>(B.flat.data()), B.flat.data(), p, B.n, h->dt, divisor, false,
+                        0, algo == DDP_ALGO_FUSED_TMA, stream));
+    }
+  }
+  for (auto& B : h->buckets) {
+    const int32_t m = static_cast<int32_t>(B.members.size());
+    SegBatcher sb(h->dt, 1.0f, stream);
+    for (int32_t r = 0; r < p; ++r)
+      for (int32_t j = 0; j < m; ++j)
+        DDP_TRY(sb.add(static_cast<const char*>(B.flat[r]) + B.offset[j] * es,
+                       const_cast<void*>(B.grads[static_cast<int64_t>(r) * m + j]), B.numel[j] * es));
+    DDP_TRY(sb.flush());
+  }
+  return DDP_OK;
+}
+
+ddp_status ddp_reducer_destroy(ddp_reducer* h) {
+  if (!h) return DDP_OK;
+  cudaError_t e = cudaSuccess;
+  for (void* a : h->arenas) {
+    const cudaError_t e2 = cudaFree(a);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (h->ws) {
+    const cudaError_t e2 = cudaFree(h->ws);
+    if (e == cudaSuccess) e = e2;
+  }
+  delete h;
+  if (e != cudaSuccess) return cuda_fail(e, "reducer release");
+  return DDP_OK;
 }
 
 ddp_status ddp_ring_create(ddp_ring** handle, ddp_op op, void* const* in, void* const* out, int32_t p,

@@ -96,6 +96,26 @@ struct StagedArgs {
   int64_t timeout_ns;          // bound of every wait on a bulk copy
 };
 
+// Bucket all-reduce straight on the gradients (flatten + all-reduce +
+// unflatten in one pass). A bucket's virtual flat layout is cut into pieces:
+// the intersections of its tensors with its chunks, so each piece has one
+// summation origin (its chunk index). ptr[slot * p + r] is replica r's tensor
+// in local slot `slot`; piece i covers elements [start, start + len) of that
+// tensor; tile0 is the prefix of each piece's tiles of kBucketTile elements.
+constexpr int kBucketPtrs = 1024;
+constexpr int kBucketPieces = 256;
+constexpr int kBucketTileBytes = 16384;
+struct BucketArgs {
+  void* ptr[kBucketPtrs];
+  int64_t start[kBucketPieces];
+  int64_t len[kBucketPieces];
+  int32_t slot[kBucketPieces];
+  int32_t origin[kBucketPieces];
+  int32_t tile0[kBucketPieces + 1];
+  int npieces, p;
+  float divisor;
+};
+
 // Literal reduce-scatter step. x[r]: replica r's input (const except in the
 // fp32 in-place all-reduce); w: fp32 partials [2][p][cs]; out[d]: where the
 // last step writes (at chunk-relative index if out_rel, else at i).

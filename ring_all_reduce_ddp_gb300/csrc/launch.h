@@ -13,6 +13,7 @@ int64_t launches();
 cudaError_t launch_fused_reduce(const FusedArgs& a, ddp_dtype dt, bool staged, cudaStream_t s);
 cudaError_t launch_rs_step_inplace_f32(const RingStepArgs& a, cudaStream_t s);
 cudaError_t launch_rs_step_ws(const RingStepArgs& a, ddp_dtype dt, cudaStream_t s);
+cudaError_t launch_bucket_allreduce(const BucketArgs& a, ddp_dtype dt, cudaStream_t s);
 cudaError_t launch_pair_copy(const PairCopyArgs& a, cudaStream_t s);
 cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s);
 cudaError_t launch_seg_copy(const SegCopyArgs& a, ddp_dtype dt, cudaStream_t s);

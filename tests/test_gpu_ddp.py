@@ -221,40 +221,110 @@ def _check_sync_sampled(cfg, red, grads, rng, per_bucket=2000):
     return True
 
 
-@pytest.mark.parametrize("algo", [D.DDP_ALGO_FUSED, D.DDP_ALGO_RING_STEPS])
-def test_tiny_ddp_sync_full_parity(algo):
-    """Ten odd-sized tensors, p = 4: flatten, all-reduce, unflatten; every element."""
-    cfg = W.CONFIGS["tiny"]
+SYNCS = [(D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE), (D.DDP_ALGO_FUSED, D.DDP_SYNC_FLATTEN),
+         (D.DDP_ALGO_FUSED_TMA, D.DDP_SYNC_FLATTEN), (D.DDP_ALGO_RING_STEPS, D.DDP_SYNC_FLATTEN)]
+
+
+def _tiny_expected(cfg, red):
+    """Oracle: flatten, literal ring all-reduce, unflatten, per bucket; tensor -> values per replica."""
     p = cfg["p"]
-    grads, _ = W.make_grads(cfg)
-    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
-    assert red.buckets == [[9, 8], [7, 6, 5, 4, 3, 2, 1, 0]]
-    red.sync_gradients(W.divisor(cfg), algo)
-    torch.cuda.synchronize()
     numel = W.numels(cfg)
     starts = W.tensor_starts(cfg)
+    out = [dict() for _ in range(p)]
     for b, members in enumerate(red.buckets):
         n = red.bucket_numel[b]
         ins = []
         for r in range(p):
             hv = {t: W.host_values(cfg, r, np.arange(starts[t], starts[t] + numel[t])) for t in members}
+            if cfg["dtype"] == "bf16":
+                hv = {t: bf16_to_f32(v) for t, v in hv.items()}
             ins.append(ob.flatten([hv.get(t, np.zeros(0, np.float32)) for t in range(len(numel))], members,
                                   red.offset, n))
-        want, _ = orc.allreduce(ins, n, W.divisor(cfg))
+        if cfg["dtype"] == "bf16":
+            from oracle.bf16 import f32_to_bf16
+            ins = [f32_to_bf16(x) for x in ins]
+        want, _ = orc.allreduce(ins, n, W.divisor(cfg), cfg["dtype"])
         for r in range(p):
-            back = ob.unflatten(want[r], members, red.offset, numel)
-            for t in members:
-                assert_bit_equal(to_host(grads[r][t]), back[t], f"tensor {t} replica {r}")
+            out[r].update(ob.unflatten(want[r], members, red.offset, numel))
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo,mode", SYNCS)
+def test_tiny_ddp_sync_full_parity(algo, mode, dtype):
+    """Ten odd-sized tensors, p = 4: every element of every gradient after one sync."""
+    cfg = dict(W.CONFIGS["tiny"], dtype=dtype)
+    p = cfg["p"]
+    grads, _ = W.make_grads(cfg)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    if dtype == "f32":
+        assert red.buckets == [[9, 8], [7, 6, 5, 4, 3, 2, 1, 0]]
+    red.sync_gradients(W.divisor(cfg), algo, mode)
+    torch.cuda.synchronize()
+    want = _tiny_expected(cfg, red)
+    for r in range(p):
+        for t in range(len(grads[r])):
+            assert_bit_equal(to_host(grads[r][t]), want[r][t], f"tensor {t} replica {r}")
     assert D.ddp_device_error() == 0
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("p", [1, 2, 3, 4, 8, 16, 17, 64])
+def test_bucket_allreduce_in_place_matches_flatten_path_oracle(p, dtype):
+    """One bucket of odd tensors (some spanning several chunks, some inside one,
+    a zero-size one, misaligned offsets) reduced straight on the gradients."""
+    rng = np.random.default_rng(p)
+    sizes = [int(x) for x in rng.integers(0, 3000, size=12)] + [0, 1, 5, 40000]
+    order = list(range(len(sizes)))[::-1]
+    offset = {}
+    pos = 0
+    for t in order:
+        offset[t] = pos
+        pos += sizes[t]
+    n = pos
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    grads, hosts = [], []
+    import synth
+    for r in range(p):
+        row, hrow = [], []
+        for t, sz in enumerate(sizes):
+            base = torch.empty(sz + 3, dtype=tdt, device="cuda")
+            v = base[(t % 3):(t % 3) + sz]  # misaligned starts, the same on every replica
+            if sz:
+                synth.fill_(v, "normal", 77, r * 100 + t)
+            row.append(v)
+            hrow.append(synth.values_np("normal", 77, r * 100 + t, np.arange(sz), 1.0, dtype))
+        grads.append(row)
+        hosts.append(hrow)
+    members = order
+    D.ddp_bucket_allreduce([[grads[r][t] for t in members] for r in range(p)], [sizes[t] for t in members],
+                           [offset[t] for t in members], tdt, float(p))
+    torch.cuda.synchronize()
+    off_list = [offset.get(t, 0) for t in range(len(sizes))]
+    ins = []
+    for r in range(p):
+        wide = [bf16_to_f32(h) if dtype == "bf16" else h for h in hosts[r]]
+        flat = ob.flatten(wide, members, off_list, n)
+        if dtype == "bf16":
+            from oracle.bf16 import f32_to_bf16
+            flat = f32_to_bf16(flat)
+        ins.append(flat)
+    want, _ = orc.allreduce(ins, n, float(p), dtype)
+    for r in range(p):
+        back = ob.unflatten(want[r], members, off_list, sizes)
+        for t in members:
+            assert_bit_equal(to_host(grads[r][t]), back[t], f"tensor {t} replica {r}")
+    assert D.ddp_device_error() == 0
+
+
+@pytest.mark.parametrize("mode", [D.DDP_SYNC_IN_PLACE, D.DDP_SYNC_FLATTEN])
 @pytest.mark.parametrize("name", ["resnet50", "gpt2_small"])
-def test_model_sized_sync_sampled_parity(name):
+def test_model_sized_sync_sampled_parity(name, mode):
     """Full-size fp32 gradient sets in the bench's launch configuration."""
     cfg = W.CONFIGS[name]
     grads, _ = W.make_grads(cfg)
     red = Reducer(grads, cfg["first_cap"], cfg["cap"])
-    red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED)
+    red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED, mode)
     torch.cuda.synchronize()
     _check_sync_sampled(cfg, red, grads, np.random.default_rng(5))
     # every replica ends identical (the data-parallel invariant), on whole tensors
