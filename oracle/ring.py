@@ -37,6 +37,10 @@ Readings where the pages leave a step open:
     chunk (q + 1) mod p, as pass 1 leaves it.
   * Byte counters count every payload at the buffer's element size, padding
     included (each reduce-scatter / all-reduce send is one cs-element chunk).
+  * Per-hop bf16 rounding (hop_round=True, bf16 only): the variant in which
+    partials travel as bf16, as a bf16 wire format would carry them: after
+    every local + received the receiver rounds the fp32 sum to bf16 (nearest
+    even); the owner then rounds fl32(sum / D) to bf16 as usual.
 """
 from __future__ import annotations
 
@@ -112,7 +116,7 @@ def _narrow(w: np.ndarray, dtype: str) -> np.ndarray:
     return f32_to_bf16(w) if dtype == "bf16" else w
 
 
-def _reduce_scatter_pass(work, chunks, p, divisor, dtype, shift, counter, snaps):
+def _reduce_scatter_pass(work, chunks, p, divisor, dtype, shift, counter, snaps, hop_round=False):
     """Pass 1: p - 1 steps; the owner's finished chunk is scaled in the last step.
 
     shift = 0: ring ownership; shift = 1: chunks pre-rotated (torch contract).
@@ -142,7 +146,10 @@ def _reduce_scatter_pass(work, chunks, p, divisor, dtype, shift, counter, snaps)
         for r, c, data in payloads:
             d = (r + 1) % p
             cols = chunks.cols[c]
-            work[d][cols] = work[d][cols] + data
+            acc = work[d][cols] + data
+            if hop_round:
+                acc = bf16_to_f32(f32_to_bf16(acc))
+            work[d][cols] = acc
             counter[r] += chunks.cs * esize
         if s == p - 2:
             scale_owned()
@@ -166,20 +173,23 @@ def _allgather_pass(work, chunks, p, owned, esize, counter, snaps):
 
 
 def allreduce(bufs, n: int, divisor: float = 1.0, dtype: str = "f32", idx=None,
-              snapshots: bool = False):
+              snapshots: bool = False, hop_round: bool = False):
     """Ring all-reduce of p replica buffers (in place in the method; here on copies).
 
     bufs: p arrays of n elements (fp32 / fp64 values or uint16 bf16 patterns), or,
     in sampled mode, of len(idx) elements holding the values at element indices idx.
     Returns (outputs, info): outputs are the p results in the input's storage type;
     info has 'bytes_sent' per rank, 'owned' chunks and, if asked, 'snapshots' (the
-    p working arrays after each of the steps, zero-padded, working precision)."""
+    p working arrays after each of the steps, zero-padded, working precision).
+    hop_round: round every partial to bf16 at each hop (bf16 buffers only)."""
+    if hop_round and dtype != "bf16":
+        raise ValueError("per-hop rounding is a bf16 variant")
     p = len(bufs)
     chunks = _Chunks(n, p, idx)
     work = _working_copies(bufs, n, chunks, dtype)
     counter = [0] * p
     snaps = [] if snapshots else None
-    owned = _reduce_scatter_pass(work, chunks, p, divisor, dtype, 0, counter, snaps)
+    owned = _reduce_scatter_pass(work, chunks, p, divisor, dtype, 0, counter, snaps, hop_round)
     _allgather_pass(work, chunks, p, owned, _ESIZE[dtype], counter, snaps)
     width = n if not chunks.sampled else chunks.width
     outs = [_narrow(w[:width], dtype) for w in work]

@@ -267,3 +267,55 @@ def test_sampled_mode_equals_full_mode():
     samp, _ = orc.allreduce([b[idx] for b in bufs], n, 8.0, idx=idx)
     for a, b in zip(full, samp):
         assert np.array_equal(a[idx], b)
+
+
+@pytest.mark.parametrize("p", [2, 4, 8])
+def test_per_hop_bf16_equals_accumulate_when_every_partial_is_exact(p):
+    """Small integers: every partial sum is a bf16 value, so rounding at each hop
+    changes nothing."""
+    rng = np.random.default_rng(p)
+    n = 257
+    vals = [rng.integers(-16, 16, size=n).astype(np.float32) for _ in range(p)]
+    bufs = [f32_to_bf16(v) for v in vals]
+    a, _ = orc.allreduce(bufs, n, 1.0, "bf16")
+    b, _ = orc.allreduce(bufs, n, 1.0, "bf16", hop_round=True)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_per_hop_bf16_worked_example():
+    """p = 8, 256 on the origin rank and 1 on the seven others. Near 256 the
+    bf16 spacing is 2, so each hop's 256 + 1 is a tie and rounds to the even
+    256: the per-hop ring ends at 256. Accumulating in fp32 gives the exact
+    263, whose single rounding (a tie between 262 and 264) goes to the even 264."""
+    p, n = 8, 8
+    bufs = []
+    for r in range(p):
+        v = np.ones(n, dtype=np.float32)
+        v[r] = 256.0  # chunk r (one element each) starts at rank r
+        bufs.append(f32_to_bf16(v))
+    hop, _ = orc.allreduce(bufs, n, 1.0, "bf16", hop_round=True)
+    acc, _ = orc.allreduce(bufs, n, 1.0, "bf16")
+    assert np.all(bf16_to_f32(hop[0]) == 256.0)
+    assert np.all(bf16_to_f32(acc[0]) == 264.0)
+
+
+def test_per_hop_bf16_error_grows_with_p():
+    """Against the exact sum, rounding every hop errs more than rounding once,
+    and more so as p grows (the error-growth study, on normal gradients)."""
+    rng = np.random.default_rng(0)
+    n = 20000
+    errs = {}
+    for p in (2, 8, 32):
+        vals = [rng.standard_normal(n).astype(np.float32) for _ in range(p)]
+        bufs = [f32_to_bf16(v) for v in vals]
+        exact = np.sum(np.stack([bf16_to_f32(b) for b in bufs]).astype(np.float64), axis=0)
+        once, _ = orc.allreduce(bufs, n, 1.0, "bf16")
+        hop, _ = orc.allreduce(bufs, n, 1.0, "bf16", hop_round=True)
+        e1 = np.mean(np.abs(bf16_to_f32(once[0]) - exact))
+        e2 = np.mean(np.abs(bf16_to_f32(hop[0]) - exact))
+        errs[p] = (e1, e2)
+        # one rounding of the exact sum: within half an ulp of bf16
+        assert np.all(np.abs(bf16_to_f32(once[0]) - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-30)
+    assert errs[2][1] >= errs[2][0] and errs[8][1] > 1.5 * errs[8][0] and errs[32][1] > 2 * errs[32][0]
+    assert errs[32][1] / errs[32][0] > errs[8][1] / errs[8][0]
