@@ -4,17 +4,18 @@ held in one GPU's memory.
 
 A step is one pass of the whole hot path on the workload's synthetic
 gradients: bucket assignment (host), the per-forward coalesced broadcast of the
-model's buffers from replica 0, then for every bucket in order flatten ->
-ring all-reduce (fused one-pass kernel by default) and finally unflatten of
-every bucket back into the gradients.
+model's buffers from replica 0, then the gradient sync of every bucket. By
+default (--mode in_place) the sync is one launch that, for every bucket,
+flattens, ring-all-reduces and unflattens in a single pass over the
+gradients; --mode flatten runs the three separate kernels per bucket.
 
 Default workload: the ResNet-50-shaped gradient set (161 fp32 tensors, 25.6M
 parameters) on p = 8 replicas, 1 MiB first bucket / 25 MiB buckets, averaged
 by 1/8, plus the broadcast of its 159 BatchNorm buffers.
 
 Prints ONE JSON line (rank 0). value = algorithmic bytes of all the step's ops
-(all-reduce 2pM, flatten 2pM, unflatten 2pM, broadcast p * buffer bytes) over
-the device-timed step, in GB/s, summed over ranks. --impl reference times the
+(all-reduce 2pM; in flatten mode also flatten 2pM and unflatten 2pM; broadcast
+p * buffer bytes) over the device-timed step, in GB/s, summed over ranks. --impl reference times the
 CPU oracle instead (on a bounded sample of the same workload).
 """
 from __future__ import annotations
@@ -49,7 +50,8 @@ WORKLOAD_TEXT = {
 # DRAM traffic of the dominant kernel (the in-place bucket all-reduce) from an
 # ncu capture, as bytes per algorithmic byte; valid only while the kernel
 # source it was taken on is unchanged (checked by hash).
-NCU_TRAFFIC = {"kernel_sha256": None, "dram_bytes_per_algorithmic_byte": None}
+NCU_TRAFFIC = {"kernel_sha256": "c9dda4587c6463d534357f1b02194bef9056d140cfcd7ebdf5f3e762bbd25a5a",
+               "dram_bytes_per_algorithmic_byte": 1575.55 / 1636.13}  # ncu: read 817.9 + write 757.7 MB per launch
 
 
 def parse_args():
@@ -193,7 +195,7 @@ def algo_code(name):
 def kernel_sha() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("k_bucket.cu", "common.cuh"):
+    for f in ("k_bucket.cu",):
         with open(os.path.join(ROOT, "ring_all_reduce_ddp_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -310,19 +312,21 @@ def run_ours(args, ranks: Ranks):
     ms_per_step = ms_max / args.steps
     value = step_bytes * args.steps * ranks.world / (ms_max / 1e3) / 1e9
 
-    # Dominant kernel: the bucket all-reduce (in place: one launch per bucket, back to back).
-    # Its duration is taken from events around each step's launches of it, so the
-    # few-microsecond gaps between consecutive launches count against it.
+    # Dominant kernel: the in-place bucket all-reduce, one launch per step over
+    # every bucket. Its duration comes from events recorded around that launch
+    # on its stream, so any launch latency the events catch counts against it.
     sync_ms = [a.elapsed_time(b) for a, b in sync_events]
     nb = len(red.buckets)
+    launches_per_sync = 1 if mode == D.DDP_SYNC_IN_PLACE else None
     achieved = ab["allreduce"] * len(sync_ms) / (sum(sync_ms) / 1e3) / 1e9
     peak, peak_kind = peak_hbm()
     traffic = None
     if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]:
-        traffic = int(NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * (ab["allreduce"] / nb))
+        traffic = int(NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * ab["allreduce"])
     bucket_mb = [round(n * esz / 2 ** 20, 2) for n in red.bucket_numel]
-    kernel_name = ("k_bucket_allreduce (flatten + ring-order all-reduce + unflatten in one pass)"
-                   if mode == D.DDP_SYNC_IN_PLACE else "flatten, fused all-reduce, unflatten (three kernels)")
+    kernel_name = ("k_bucket_allreduce_table: every bucket's flatten + ring-order all-reduce + unflatten "
+                   "in one launch" if mode == D.DDP_SYNC_IN_PLACE
+                   else "flatten, fused all-reduce, unflatten per bucket (whole sync timed)")
 
     # End to end through the public API: every replica's gradients in from pinned
     # host memory, one step, the synchronised gradients out, every step.
@@ -388,8 +392,10 @@ def run_ours(args, ranks: Ranks):
                    "parallelism": f"replicas only: {ranks.world} independent GPU(s)"},
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes_per_launch": int(ab["allreduce"] / nb),
-                     "avg_launch_us": round(1e3 * statistics.mean(sync_ms) / nb, 2)},
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": int(ab["allreduce"]) if launches_per_sync else None,
+                     "avg_launch_us": round(1e3 * statistics.mean(sync_ms), 2) if launches_per_sync else None,
+                     "avg_sync_us": round(1e3 * statistics.mean(sync_ms), 2)},
         "allreduce_gbs": round(achieved, 1),
         "buckets_per_s": round(nb * args.steps * ranks.world / (ms_max / 1e3), 1),
         "busbw_gbs": round(sum(n * esz for n in red.bucket_numel) / (statistics.mean(sync_ms) / 1e3) / 1e9

@@ -79,6 +79,9 @@ typedef enum {
                                  bucket 0, then reverse the bucket list                  */
 } ddp_border;
 
+/* Flags of ddp_allreduce_ex. */
+#define DDP_FLAG_ROUND_EACH_HOP 1u
+
 typedef enum {
   DDP_SYNC_FLATTEN = 0,  /* per bucket: flatten, all-reduce the flat bucket; then unflatten */
   DDP_SYNC_IN_PLACE = 1  /* per bucket: one pass over the gradients themselves            */
@@ -161,6 +164,39 @@ ddp_status ddp_bucket_unflatten(int32_t p, int32_t k, const void* const* bucket,
 ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype,
                          float divisor, ddp_algo algo, cudaStream_t stream);
 
+/* ddp_allreduce with variant flags (0 gives ddp_allreduce exactly).
+ *   DDP_FLAG_ROUND_EACH_HOP (bf16 only, else DDP_ERR_DTYPE): the partials
+ *   travel as bf16, as a bf16 wire format would carry them ([COLL] "Ring
+ *   allreduce in two passes": the receiver accumulates the received chunk into
+ *   its local copy, here a bf16 copy). After every local + received (an fp32
+ *   add) the sum is rounded to bf16; the owner's y = RNE_bf16(fl32(sum / D)).
+ *   Literal (RING_STEPS) and fused forms give the same bits; _FUSED_TMA runs
+ *   the register-path kernel for this variant. */
+ddp_status ddp_allreduce_ex(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
+                            ddp_algo algo, uint32_t flags, cudaStream_t stream);
+
+/* The literal 2(p-1)-step ring as one persistent cooperative kernel with
+ * device-side step synchronisation, bounded waits and host-set fault
+ * injection. [COLL] "Ring allreduce in two passes" (rank r receives from
+ * r - 1 each step) and its exercise on a configurable receive timeout that
+ * surfaces a deadline error instead of waiting forever.
+ * Same result as ddp_allreduce, bit for bit (fp32 only, else DDP_ERR_DTYPE).
+ * Each simulated rank gets blocks of its own; receiver d waits, before step t,
+ * until its sender d-1 has posted t steps. A wait gives up after timeout_ns
+ * (0 means 1 s); the kernel then records the failure and ends (no trap).
+ *   fault_rank, fault_step: inject "rank fault_rank never posts step
+ *     fault_step" (it stops before that step); -1 for no fault.
+ *   status: NULL, or 4 device int32 words the caller owns, zeroed by the call
+ *     and written by the kernel: {0 or DDP_ERR_TIMEOUT, the rank whose wait
+ *     gave up first, the step it waited for, number of waits that gave up}.
+ * A wait that ran out also sets the library's device error word
+ * (ddp_device_error returns DDP_ERR_TIMEOUT). Buffers are then only partly
+ * reduced. Needs p co-resident blocks (DDP_ERR_ARG otherwise); the step flags
+ * are a stream-ordered temporary. */
+ddp_status ddp_allreduce_persistent(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
+                                    int64_t timeout_ns, int32_t fault_rank, int32_t fault_step,
+                                    int32_t* status, cudaStream_t stream);
+
 /* Reduce-scatter: pass 1 alone. [COLL] code/main.py list (reduce_scatter
  * pre-rotates so rank r returns the sum of chunk r and rejects element counts
  * not divisible by the world size); [DP] "The collective operations".
@@ -233,8 +269,9 @@ ddp_status ddp_bucket_allreduce(int32_t p, int32_t k, void* const* grads, const 
  *   DDP_SYNC_FLATTEN: for every bucket in order, ddp_bucket_flatten (with
  *     predivide) then ddp_allreduce with `algo`; then ddp_bucket_unflatten of
  *     every bucket ([DDP] "Step 3: finalize_backward").
- *   DDP_SYNC_IN_PLACE: for every bucket in order, ddp_bucket_allreduce
- *     (fused algos only; predivide must be 1).
+ *   DDP_SYNC_IN_PLACE: every bucket's ddp_bucket_allreduce, all in ONE launch
+ *     driven by a piece table uploaded to device memory at create (fused
+ *     algos only; predivide must be 1). Tiles are ordered bucket by bucket.
  * Both give the same bits. */
 typedef struct ddp_reducer ddp_reducer;
 ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* const* grads,

@@ -29,6 +29,8 @@ DDP_ALGO_FUSED, DDP_ALGO_RING_STEPS, DDP_ALGO_FUSED_LDST, DDP_ALGO_FUSED_TMA = 0
 DDP_OWN_RANK, DDP_OWN_RING = 0, 1
 # ddp_border
 DDP_ORDER_REVERSED, DDP_ORDER_REGISTRATION = 0, 1
+# flags of ddp_allreduce_ex
+DDP_FLAG_ROUND_EACH_HOP = 1
 # ddp_sync_mode
 DDP_SYNC_FLATTEN, DDP_SYNC_IN_PLACE = 0, 1
 # ddp_op
@@ -46,6 +48,8 @@ _SIGS = {
     "ddp_bucket_flatten": [_c_i32, _c_i32, _P_vp, _P_i64, _P_i64, _P_vp, _c_i32, _c_f32, _c_vp],
     "ddp_bucket_unflatten": [_c_i32, _c_i32, _P_vp, _P_i64, _P_i64, _P_vp, _c_i32, _c_vp],
     "ddp_allreduce": [_P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32, _c_vp],
+    "ddp_allreduce_persistent": [_P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i64, _c_i32, _c_i32, _c_vp, _c_vp],
+    "ddp_allreduce_ex": [_P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32, ctypes.c_uint32, _c_vp],
     "ddp_reduce_scatter": [_P_vp, _P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32, _c_i32, _c_vp],
     "ddp_allgather": [_P_vp, _P_vp, _c_i32, _c_i64, _c_i32, _c_i32, _c_i32, _c_vp],
     "ddp_bucket_allreduce": [_c_i32, _c_i32, _P_vp, _P_i64, _P_i64, _c_i32, _c_f32, _c_vp],
@@ -201,6 +205,20 @@ def ddp_allreduce(bufs, n: int, dtype=DDP_FLOAT32, divisor: float = 1.0, algo: i
                   stream=None):
     _check(lib().ddp_allreduce(_ptrs(bufs), len(bufs), int(n), _dtype(dtype), float(divisor), algo,
                                _stream(stream)))
+
+
+def ddp_allreduce_ex(bufs, n: int, dtype=DDP_FLOAT32, divisor: float = 1.0, algo: int = DDP_ALGO_FUSED,
+                     flags: int = 0, stream=None):
+    _check(lib().ddp_allreduce_ex(_ptrs(bufs), len(bufs), int(n), _dtype(dtype), float(divisor), algo,
+                                  int(flags), _stream(stream)))
+
+
+def ddp_allreduce_persistent(bufs, n: int, dtype=DDP_FLOAT32, divisor: float = 1.0, timeout_ns: int = 0,
+                             fault_rank: int = -1, fault_step: int = 0, status=None, stream=None):
+    """status: None or a device int32 tensor of 4 words (zeroed and written by the call)."""
+    _check(lib().ddp_allreduce_persistent(_ptrs(bufs), len(bufs), int(n), _dtype(dtype), float(divisor),
+                                          int(timeout_ns), int(fault_rank), int(fault_step), _ptr(status),
+                                          _stream(stream)))
 
 
 def ddp_reduce_scatter(ins, outs, n: int, dtype=DDP_FLOAT32, divisor: float = 1.0, own: int = DDP_OWN_RANK,

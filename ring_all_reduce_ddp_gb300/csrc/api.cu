@@ -87,7 +87,8 @@ bool same_align16(const void* const* v, int32_t count) {
 
 // Fused one-pass reduction of p replicas.
 ddp_status run_fused(const void* const* in, void* const* out, int32_t p, int64_t n, ddp_dtype dt,
-                     float divisor, bool scatter, int shift, bool staged, cudaStream_t s) {
+                     float divisor, bool scatter, int shift, bool staged, cudaStream_t s,
+                     bool hop_round = false) {
   FusedArgs a;
   std::memset(&a, 0, sizeof(a));
   for (int j = 0; j < 2 * p; ++j) a.src[j] = in[j % p];
@@ -101,6 +102,7 @@ ddp_status run_fused(const void* const* in, void* const* out, int32_t p, int64_t
   // All-reduce reads and writes the same p replicas; a scatter's outputs are
   // checked per chunk in the kernel.
   a.same_align = same_align16(in, p) ? 1 : 0;
+  a.hop_round = hop_round ? 1 : 0;
   DDP_CUDA(launch_fused_reduce(a, dt, staged, s), "fused reduction launch");
   return DDP_OK;
 }
@@ -118,6 +120,7 @@ struct Plan {
   int64_t cs = 0;
   float* ws = nullptr;
   bool ws_async = false;
+  bool hop_round = false;  // bf16 all-reduce: round every partial to bf16
   int32_t nsteps = 0, done = 0;
   std::vector<int64_t> sent;
 
@@ -155,7 +158,7 @@ struct Plan {
         std::memset(&a, 0, sizeof(a));
         for (int r = 0; r < p; ++r) { a.x[r] = in[r]; a.out[r] = in[r]; }
         a.w = ws; a.n = n; a.cs = cs; a.divisor = divisor; a.p = p; a.step = st;
-        a.shift = 0; a.last = (st == p - 2); a.out_rel = 0;
+        a.shift = 0; a.last = (st == p - 2); a.out_rel = 0; a.hop_round = hop_round ? 1 : 0;
         DDP_CUDA(dt == DDP_FLOAT32 ? launch_rs_step_inplace_f32(a, s) : launch_rs_step_ws(a, dt, s),
                  "reduce-scatter step launch");
         for (int r = 0; r < p; ++r) sent[r] += cs * es;
@@ -502,9 +505,17 @@ ddp_status ddp_bucket_unflatten(int32_t p, int32_t k, const void* const* bucket,
 
 ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
                          ddp_algo algo, cudaStream_t stream) {
+  return ddp_allreduce_ex(bufs, p, n, dtype, divisor, algo, 0u, stream);
+}
+
+ddp_status ddp_allreduce_ex(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
+                            ddp_algo algo, uint32_t flags, cudaStream_t stream) {
   DDP_TRY(check_common(p, n, dtype));
   DDP_TRY(check_divisor(divisor));
   DDP_TRY(check_algo(algo));
+  DDP_CHECK((flags & ~static_cast<uint32_t>(DDP_FLAG_ROUND_EACH_HOP)) == 0, DDP_ERR_ARG, "unknown flags");
+  const bool hop = (flags & DDP_FLAG_ROUND_EACH_HOP) != 0;
+  DDP_CHECK(!hop || dtype == DDP_BFLOAT16, DDP_ERR_DTYPE, "DDP_FLAG_ROUND_EACH_HOP is a bf16 variant");
   DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
   const int es = esize(dtype);
   std::vector<std::pair<uintptr_t, uintptr_t>> rg;
@@ -513,12 +524,12 @@ ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtyp
   if (n == 0) return DDP_OK;
   if (algo == DDP_ALGO_RING_STEPS) {
     Plan pl;
-    pl.op = DDP_OP_ALLREDUCE; pl.p = p; pl.n = n; pl.dt = dtype; pl.divisor = divisor;
+    pl.op = DDP_OP_ALLREDUCE; pl.p = p; pl.n = n; pl.dt = dtype; pl.divisor = divisor; pl.hop_round = hop;
     pl.in.assign(bufs, bufs + p);
     return run_plan_once(pl, stream);
   }
   return run_fused(const_cast<const void* const*>(bufs), bufs, p, n, dtype, divisor, false, 0,
-                   algo == DDP_ALGO_FUSED_TMA, stream);
+                   algo == DDP_ALGO_FUSED_TMA && !hop, stream, hop);
 }
 
 ddp_status ddp_reduce_scatter(const void* const* in, void* const* out, int32_t p, int64_t n, ddp_dtype dtype,
@@ -774,13 +785,80 @@ struct ddp_reducer {
     int64_t n = 0;
     std::vector<void*> flat;             // [p]
     std::vector<const void*> grads;      // [p * members], replica-major
-    std::vector<BucketArgs> in_place;    // prebuilt launches
   };
   std::vector<Bucket> buckets;
   std::vector<void*> arenas;  // one flat-bucket arena per replica
   float* ws = nullptr;        // fp32 partials for the literal bf16 schedule
   int64_t ws_elems = 0;
+  void* table_mem = nullptr;  // the in-place sync's piece table, every bucket, in device memory
+  BucketTable table{};
+  int32_t table_tiles = 0;
 };
+
+namespace {
+
+// Cut every bucket of the reducer into pieces (tensor x chunk, one summation
+// origin each), in bucket order, and upload the table to device memory once.
+ddp_status build_reducer_table(ddp_reducer* h) {
+  const int p = h->p;
+  const int64_t tile = kBucketTileBytes / esize(h->dt);
+  std::vector<void*> ptr;
+  std::vector<int64_t> start, len;
+  std::vector<int32_t> slot, origin, tile0{0};
+  int32_t nslots = 0;
+  for (const auto& B : h->buckets) {
+    if (B.n == 0) continue;
+    const int64_t cs = chunk_size(B.n, p);
+    const int32_t m = static_cast<int32_t>(B.members.size());
+    for (int32_t j = 0; j < m; ++j) {
+      if (B.numel[j] == 0) continue;
+      const int32_t sl = nslots++;
+      for (int r = 0; r < p; ++r) ptr.push_back(const_cast<void*>(B.grads[static_cast<int64_t>(r) * m + j]));
+      const int64_t lo = B.offset[j], hi = B.offset[j] + B.numel[j];
+      for (int64_t c = lo / cs; c <= (hi - 1) / cs; ++c) {
+        const int64_t plo = std::max(lo, c * cs), phi = std::min(hi, (c + 1) * cs);
+        start.push_back(plo - lo);
+        len.push_back(phi - plo);
+        slot.push_back(sl);
+        origin.push_back(static_cast<int32_t>(c));
+        const int64_t t = static_cast<int64_t>(tile0.back()) + (phi - plo + tile - 1) / tile;
+        DDP_CHECK(t <= 0x7FFFFFFF, DDP_ERR_ARG, "gradient set too large for one in-place launch");
+        tile0.push_back(static_cast<int32_t>(t));
+      }
+    }
+  }
+  const size_t np = start.size();
+  if (np == 0) return DDP_OK;
+  auto up16 = [](size_t x) { return (x + 15) / 16 * 16; };
+  const size_t o_ptr = 0, o_start = up16(o_ptr + ptr.size() * sizeof(void*)), o_len = up16(o_start + np * 8),
+               o_slot = up16(o_len + np * 8), o_origin = up16(o_slot + np * 4), o_tile0 = up16(o_origin + np * 4),
+               total = up16(o_tile0 + (np + 1) * 4);
+  std::vector<unsigned char> host(total, 0);
+  std::memcpy(host.data() + o_ptr, ptr.data(), ptr.size() * sizeof(void*));
+  std::memcpy(host.data() + o_start, start.data(), np * 8);
+  std::memcpy(host.data() + o_len, len.data(), np * 8);
+  std::memcpy(host.data() + o_slot, slot.data(), np * 4);
+  std::memcpy(host.data() + o_origin, origin.data(), np * 4);
+  std::memcpy(host.data() + o_tile0, tile0.data(), (np + 1) * 4);
+  void* mem = nullptr;
+  cudaError_t e = cudaMalloc(&mem, total);
+  if (e != cudaSuccess) return fail(DDP_ERR_NOMEM, std::string("reducer piece table: ") + cudaGetErrorString(e));
+  h->table_mem = mem;
+  DDP_CUDA(cudaMemcpy(mem, host.data(), total, cudaMemcpyHostToDevice), "reducer piece table upload");
+  unsigned char* d = static_cast<unsigned char*>(mem);
+  h->table.ptr = reinterpret_cast<void* const*>(d + o_ptr);
+  h->table.start = reinterpret_cast<const int64_t*>(d + o_start);
+  h->table.len = reinterpret_cast<const int64_t*>(d + o_len);
+  h->table.slot = reinterpret_cast<const int32_t*>(d + o_slot);
+  h->table.origin = reinterpret_cast<const int32_t*>(d + o_origin);
+  h->table.tile0 = reinterpret_cast<const int32_t*>(d + o_tile0);
+  h->table.npieces = static_cast<int>(np);
+  h->table.p = p;
+  h->table_tiles = tile0.back();
+  return DDP_OK;
+}
+
+}  // namespace
 
 ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* const* grads,
                               const int64_t* numel, ddp_dtype dtype, int64_t first_bucket_cap_bytes,
@@ -820,6 +898,7 @@ ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* 
   auto fail_free = [&](ddp_status st, const std::string& msg) {
     for (void* a : h->arenas) cudaFree(a);
     if (h->ws) cudaFree(h->ws);
+    if (h->table_mem) cudaFree(h->table_mem);
     delete h;
     return fail(st, msg);
   };
@@ -849,10 +928,11 @@ ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* 
       B.flat.push_back(static_cast<char*>(h->arenas[r]) + base[b]);
       for (int32_t t : B.members) B.grads.push_back(grads[static_cast<int64_t>(r) * k + t]);
     }
-    const ddp_status st = plan_bucket_launches(p, m, B.grads.data(), B.numel.data(), B.offset.data(), dtype, 1.0f,
-                                               B.in_place);
-    if (st != DDP_OK) return fail_free(st, t_error);
     h->buckets.push_back(std::move(B));
+  }
+  {
+    const ddp_status st = build_reducer_table(h);
+    if (st != DDP_OK) return fail_free(st, t_error);
   }
   *handle = h;
   return DDP_OK;
@@ -880,7 +960,7 @@ ddp_status ddp_reducer_sync(ddp_reducer* h, float divisor, float predivide, ddp_
   if (mode == DDP_SYNC_IN_PLACE) {
     DDP_CHECK(algo != DDP_ALGO_RING_STEPS, DDP_ERR_ARG, "the in-place sync is the fused form only");
     DDP_CHECK(predivide == 1.0f, DDP_ERR_ARG, "the in-place sync has no pre-divide");
-    for (auto& B : h->buckets) DDP_TRY(run_bucket_launches(B.in_place, h->dt, divisor, stream));
+    DDP_CUDA(launch_bucket_table(h->table, h->table_tiles, divisor, h->dt, stream), "in-place sync launch");
     return DDP_OK;
   }
   const int es = esize(h->dt);
@@ -928,8 +1008,55 @@ ddp_status ddp_reducer_destroy(ddp_reducer* h) {
     const cudaError_t e2 = cudaFree(h->ws);
     if (e == cudaSuccess) e = e2;
   }
+  if (h->table_mem) {
+    const cudaError_t e2 = cudaFree(h->table_mem);
+    if (e == cudaSuccess) e = e2;
+  }
   delete h;
   if (e != cudaSuccess) return cuda_fail(e, "reducer release");
+  return DDP_OK;
+}
+
+
+ddp_status ddp_allreduce_persistent(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
+                                    int64_t timeout_ns, int32_t fault_rank, int32_t fault_step, int32_t* status,
+                                    cudaStream_t stream) {
+  DDP_TRY(check_common(p, n, dtype));
+  DDP_CHECK(dtype == DDP_FLOAT32, DDP_ERR_DTYPE, "the persistent ring runs fp32 buffers");
+  DDP_TRY(check_divisor(divisor));
+  DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
+  DDP_CHECK(timeout_ns >= 0, DDP_ERR_ARG, "timeout_ns must be >= 0");
+  const int32_t T = 2 * (p - 1);
+  DDP_CHECK(fault_rank == -1 || (fault_rank >= 0 && fault_rank < p && fault_step >= 0 && fault_step < T),
+            DDP_ERR_ARG, "fault_rank must be -1 or a rank, fault_step a step in [0, 2(p-1))");
+  std::vector<std::pair<uintptr_t, uintptr_t>> rg;
+  for (int r = 0; r < p; ++r) rg.push_back(range_of(bufs[r], n * 4));
+  DDP_CHECK(disjoint(rg), DDP_ERR_ARG, "replica buffers overlap");
+  if (status) DDP_CUDA(cudaMemsetAsync(status, 0, 4 * sizeof(int32_t), stream), "status reset");
+  if (n == 0) return DDP_OK;
+  if (p == 1) return run_fused(const_cast<const void* const*>(bufs), bufs, 1, n, dtype, divisor, false, 0, false,
+                               stream);
+  const int max_blocks = ring_persistent_max_blocks();
+  DDP_CHECK(max_blocks >= p, DDP_ERR_ARG, "more ranks than co-resident blocks for the persistent ring");
+  const int64_t cs = chunk_size(n, p);
+  int B = max_blocks / p;
+  const int64_t useful = std::max<int64_t>(1, (cs + kThreads * 4 - 1) / (kThreads * 4));
+  if (B > useful) B = static_cast<int>(useful);
+  PersistArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) a.buf[r] = bufs[r];
+  a.n = n; a.cs = cs; a.divisor = divisor; a.p = p; a.blocks_per_rank = B;
+  a.fault_rank = fault_rank; a.fault_step = fault_step;
+  a.timeout_ns = timeout_ns > 0 ? timeout_ns : 1000000000LL;
+  a.status = status;
+  void* flags = nullptr;
+  DDP_CUDA(cudaMallocAsync(&flags, static_cast<size_t>(p) * B * sizeof(int), stream), "step flags allocation");
+  a.flags = static_cast<int*>(flags);
+  cudaError_t e = cudaMemsetAsync(flags, 0, static_cast<size_t>(p) * B * sizeof(int), stream);
+  if (e == cudaSuccess) e = launch_ring_persistent(a, stream);
+  const cudaError_t e2 = cudaFreeAsync(flags, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "persistent ring launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "step flags release");
   return DDP_OK;
 }
 

@@ -29,6 +29,10 @@ template <> __device__ __forceinline__ __nv_bfloat16 narrow<__nv_bfloat16>(float
   return __float2bfloat16_rn(x);
 }
 
+// The fp32 value rounded to bf16 (nearest even) and widened back: what a
+// partial becomes when it is stored as bf16 between hops.
+__device__ __forceinline__ float round_bf16(float x) { return widen(__float2bfloat16_rn(x)); }
+
 // A 16-byte vector seen as N fp32 lanes.
 template <typename T> struct Vec;
 template <> struct Vec<float> {
@@ -76,6 +80,7 @@ struct FusedArgs {
   int scatter;       // 0: write y to every dst at index i; 1: to dst[owner] at i - c*cs
   int shift;         // origin of chunk c is (c + shift) mod p
   int same_align;    // every src / dst base has the same address mod 16
+  int hop_round;     // bf16 only: round each partial to bf16 after every add
 };
 
 // Fused reduction staged through shared memory by bulk (TMA) copies. Chunk c's
@@ -116,6 +121,18 @@ struct BucketArgs {
   float divisor;
 };
 
+// The same piece table held in device memory (a Reducer's whole set of
+// buckets, uploaded once): arrays of npieces entries, ptr of (slots * p).
+struct BucketTable {
+  void* const* ptr;
+  const int64_t* start;
+  const int64_t* len;
+  const int32_t* slot;
+  const int32_t* origin;
+  const int32_t* tile0;  // npieces + 1 entries
+  int npieces, p;
+};
+
 // Literal reduce-scatter step. x[r]: replica r's input (const except in the
 // fp32 in-place all-reduce); w: fp32 partials [2][p][cs]; out[d]: where the
 // last step writes (at chunk-relative index if out_rel, else at i).
@@ -126,6 +143,21 @@ struct RingStepArgs {
   int64_t n, cs;
   float divisor;
   int p, step, shift, last, out_rel;
+  int hop_round;  // bf16 only: round each partial to bf16 after every add
+};
+
+// Persistent literal ring (fp32, in place): every rank's blocks in one
+// cooperative launch; block b of rank d handles slice b of each step's chunk
+// and waits for block b of rank d-1 to have posted the previous step.
+struct PersistArgs {
+  void* buf[kMaxP];
+  int* flags;          // [p][blocks_per_rank]: steps posted; zero at launch
+  int* status;         // caller's 4 device words, or null: {code, rank, step, waits that gave up}
+  int64_t n, cs;
+  float divisor;
+  int p, blocks_per_rank;
+  int fault_rank, fault_step;  // injected: that rank never posts that step (-1: none)
+  int64_t timeout_ns;          // bound of every wait
 };
 
 // Copy jobs: job j copies nbytes[j] bytes from src[j] to dst[j].

@@ -9,13 +9,23 @@
 // tensor in slot s sits at bucket position offset_s + e, which belongs to
 // chunk c = position / ceil(n/p) and is therefore summed starting at rank c,
 // ((x_c + x_{c+1}) + ...) + x_{c+p-1}, then divided once by the divisor: the
-// same bits as the ring on the flat bucket.
+// same bits as the ring on the flat bucket. Work is cut into pieces (a tensor
+// intersected with a chunk: one origin each) and pieces into tiles of
+// kBucketTileBytes per replica; a persistent grid strides over the tiles.
 #include "launch.h"
 
 namespace ddp {
 namespace {
 
-constexpr int kVecPerThread = kBucketTileBytes / 16 / kThreads;  // 4
+struct View {
+  void* const* ptr;
+  const int64_t* start;
+  const int64_t* len;
+  const int32_t* slot;
+  const int32_t* origin;
+  const int32_t* tile0;
+  int npieces, p;
+};
 
 __device__ __forceinline__ int find_piece(const int32_t* tile0, int n, int32_t b) {
   int lo = 0, hi = n;  // tile0[lo] <= b < tile0[hi]
@@ -27,23 +37,21 @@ __device__ __forceinline__ int find_piece(const int32_t* tile0, int n, int32_t b
 }
 
 template <typename T, int P>
-__global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_constant__ BucketArgs a) {
+__device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divisor) {
   constexpr int V = Vec<T>::N;
   constexpr int64_t kTile = kBucketTileBytes / sizeof(T);
   const int p = (P > 0) ? P : a.p;
-  const int32_t b = blockIdx.x;
   const int i = find_piece(a.tile0, a.npieces, b);
-  const int64_t t0 = a.start[i] + static_cast<int64_t>(b - a.tile0[i]) * kTile;  // first element of this tile
+  const int64_t t0 = a.start[i] + static_cast<int64_t>(b - a.tile0[i]) * kTile;  // first element of the tile
   const int64_t len = min(kTile, a.start[i] + a.len[i] - t0);
   if (len <= 0) return;
-  void* const* rep = &a.ptr[static_cast<int64_t>(a.slot[i]) * p];
+  void* const* rep = a.ptr + static_cast<int64_t>(a.slot[i]) * p;
   const int o = a.origin[i];
 
-  // the ring order o, o+1, ..., o+p-1 (mod p) as replica indices
-  int order[P > 0 ? P : 1];
+  T* base[P > 0 ? P : 1];  // replicas in ring order o, o+1, ... (mod p)
   if constexpr (P > 0) {
 #pragma unroll
-    for (int j = 0; j < P; ++j) order[j] = (o + j) % P;
+    for (int j = 0; j < P; ++j) base[j] = reinterpret_cast<T*>(rep[(o + j) % P]);
   }
 
   // a vector path needs every replica at the same address mod 16
@@ -56,7 +64,6 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_cons
   const int64_t nvec = (len - head) / V;
   const int64_t tail0 = head + nvec * V;
 
-  // scalar elements: the head, the tail, or all of them
   for (int64_t e = threadIdx.x; e < head + (len - tail0); e += blockDim.x) {
     const int64_t x = t0 + (e < head ? e : tail0 + (e - head));
     float acc = widen(reinterpret_cast<const T*>(rep[o])[x]);
@@ -65,7 +72,7 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_cons
       r = (r + 1 == p) ? 0 : r + 1;
       acc = __fadd_rn(acc, widen(reinterpret_cast<const T*>(rep[r])[x]));
     }
-    const T y = narrow<T>(__fdiv_rn(acc, a.divisor));
+    const T y = narrow<T>(__fdiv_rn(acc, divisor));
     for (int q = 0; q < p; ++q) reinterpret_cast<T*>(rep[q])[x] = y;
   }
 
@@ -75,7 +82,7 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_cons
     if constexpr (P > 0) {
       uint4 w[P];
 #pragma unroll
-      for (int j = 0; j < P; ++j) w[j] = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(rep[order[j]]) + x);
+      for (int j = 0; j < P; ++j) w[j] = *reinterpret_cast<const uint4*>(base[j] + x);
       Vec<T>::unpack(w[0], acc);
 #pragma unroll
       for (int j = 1; j < P; ++j) {
@@ -85,10 +92,10 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_cons
         for (int l = 0; l < V; ++l) acc[l] = __fadd_rn(acc[l], t[l]);
       }
 #pragma unroll
-      for (int l = 0; l < V; ++l) acc[l] = __fdiv_rn(acc[l], a.divisor);
+      for (int l = 0; l < V; ++l) acc[l] = __fdiv_rn(acc[l], divisor);
       const uint4 y = Vec<T>::pack(acc);
 #pragma unroll
-      for (int q = 0; q < P; ++q) *reinterpret_cast<uint4*>(reinterpret_cast<T*>(rep[q]) + x) = y;
+      for (int q = 0; q < P; ++q) *reinterpret_cast<uint4*>(base[q] + x) = y;
     } else {
       Vec<T>::unpack(*reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(rep[o]) + x), acc);
       int r = o;
@@ -100,22 +107,81 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_cons
         for (int l = 0; l < V; ++l) acc[l] = __fadd_rn(acc[l], t[l]);
       }
 #pragma unroll
-      for (int l = 0; l < V; ++l) acc[l] = __fdiv_rn(acc[l], a.divisor);
+      for (int l = 0; l < V; ++l) acc[l] = __fdiv_rn(acc[l], divisor);
       const uint4 y = Vec<T>::pack(acc);
       for (int q = 0; q < p; ++q) *reinterpret_cast<uint4*>(reinterpret_cast<T*>(rep[q]) + x) = y;
     }
   }
 }
 
+template <typename T, int P>
+__device__ __forceinline__ void bucket_tiles(const View& v, float divisor) {
+  const int32_t total = v.tile0[v.npieces];
+  for (int32_t b = blockIdx.x; b < total; b += gridDim.x) bucket_tile<T, P>(v, b, divisor);
+}
+
+// Arguments by value (one bucket, from ddp_bucket_allreduce).
+template <typename T, int P>
+__global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_constant__ BucketArgs a) {
+  const View v{a.ptr, a.start, a.len, a.slot, a.origin, a.tile0, a.npieces, a.p};
+  bucket_tiles<T, P>(v, a.divisor);
+}
+
+// Piece table in device memory (every bucket of a Reducer in one launch).
+template <typename T, int P>
+__global__ void __launch_bounds__(kThreads) k_bucket_allreduce_table(const BucketTable t, float divisor) {
+  const View v{t.ptr, t.start, t.len, t.slot, t.origin, t.tile0, t.npieces, t.p};
+  bucket_tiles<T, P>(v, divisor);
+}
+
+// Persistent grid: as many blocks as fit on the device at once, at most one per
+// tile. The occupancy of each kernel instantiation is looked up once per device.
+template <typename T, int P, bool kTable>
+int persistent_grid(int32_t tiles) {
+  static int per_sm[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (per_sm[dev] == 0) {
+    int blocks = 0;
+    cudaError_t e;
+    if constexpr (kTable)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_bucket_allreduce_table<T, P>, kThreads, 0);
+    else
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_bucket_allreduce<T, P>, kThreads, 0);
+    per_sm[dev] = (e == cudaSuccess && blocks > 0) ? blocks : 1;
+  }
+  const int64_t g = static_cast<int64_t>(per_sm[dev]) * sm_count();
+  return static_cast<int>(g < tiles ? g : tiles);
+}
+
 template <typename T>
-cudaError_t bucket_launch(const BucketArgs& a, cudaStream_t s) {
+cudaError_t by_value(const BucketArgs& a, cudaStream_t s) {
   const int32_t tiles = a.tile0[a.npieces];
   switch (a.p) {
-    case 2: k_bucket_allreduce<T, 2><<<tiles, kThreads, 0, s>>>(a); break;
-    case 4: k_bucket_allreduce<T, 4><<<tiles, kThreads, 0, s>>>(a); break;
-    case 8: k_bucket_allreduce<T, 8><<<tiles, kThreads, 0, s>>>(a); break;
-    case 16: k_bucket_allreduce<T, 16><<<tiles, kThreads, 0, s>>>(a); break;
-    default: k_bucket_allreduce<T, 0><<<tiles, kThreads, 0, s>>>(a); break;
+    case 2: k_bucket_allreduce<T, 2><<<persistent_grid<T, 2, false>(tiles), kThreads, 0, s>>>(a); break;
+    case 4: k_bucket_allreduce<T, 4><<<persistent_grid<T, 4, false>(tiles), kThreads, 0, s>>>(a); break;
+    case 8: k_bucket_allreduce<T, 8><<<persistent_grid<T, 8, false>(tiles), kThreads, 0, s>>>(a); break;
+    case 16: k_bucket_allreduce<T, 16><<<persistent_grid<T, 16, false>(tiles), kThreads, 0, s>>>(a); break;
+    default: k_bucket_allreduce<T, 0><<<persistent_grid<T, 0, false>(tiles), kThreads, 0, s>>>(a); break;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <typename T, int P>
+void launch_table(const BucketTable& t, int32_t tiles, float divisor, cudaStream_t s) {
+  k_bucket_allreduce_table<T, P><<<persistent_grid<T, P, true>(tiles), kThreads, 0, s>>>(t, divisor);
+}
+
+template <typename T>
+cudaError_t by_table(const BucketTable& t, int32_t tiles, float divisor, cudaStream_t s) {
+  switch (t.p) {
+    case 2: launch_table<T, 2>(t, tiles, divisor, s); break;
+    case 4: launch_table<T, 4>(t, tiles, divisor, s); break;
+    case 8: launch_table<T, 8>(t, tiles, divisor, s); break;
+    case 16: launch_table<T, 16>(t, tiles, divisor, s); break;
+    default: launch_table<T, 0>(t, tiles, divisor, s); break;
   }
   count_launch();
   return cudaGetLastError();
@@ -125,7 +191,14 @@ cudaError_t bucket_launch(const BucketArgs& a, cudaStream_t s) {
 
 cudaError_t launch_bucket_allreduce(const BucketArgs& a, ddp_dtype dt, cudaStream_t s) {
   if (a.npieces <= 0 || a.tile0[a.npieces] <= 0) return cudaSuccess;
-  return dt == DDP_FLOAT32 ? bucket_launch<float>(a, s) : bucket_launch<__nv_bfloat16>(a, s);
+  return dt == DDP_FLOAT32 ? by_value<float>(a, s) : by_value<__nv_bfloat16>(a, s);
+}
+
+cudaError_t launch_bucket_table(const BucketTable& t, int32_t total_tiles, float divisor, ddp_dtype dt,
+                                cudaStream_t s) {
+  if (t.npieces <= 0 || total_tiles <= 0) return cudaSuccess;
+  return dt == DDP_FLOAT32 ? by_table<float>(t, total_tiles, divisor, s)
+                           : by_table<__nv_bfloat16>(t, total_tiles, divisor, s);
 }
 
 }  // namespace ddp

@@ -24,7 +24,7 @@ namespace ddp {
 __device__ int g_device_error = 0;
 
 // ------------------------------------------------ fused, register-only path
-template <typename T, int P>
+template <typename T, int P, bool HOP = false>
 __global__ void __launch_bounds__(kThreads) k_fused_reduce_ldst(const __grid_constant__ FusedArgs a) {
   const int p = (P > 0) ? P : a.p;
   const int c = blockIdx.y;
@@ -57,7 +57,10 @@ __global__ void __launch_bounds__(kThreads) k_fused_reduce_ldst(const __grid_con
   for (int64_t e = gtid; e < nscalar; e += gstride) {
     const int64_t i = lo + (e < head ? e : tail0 + (e - head));
     float acc = widen(src[0][i]);
-    for (int j = 1; j < p; ++j) acc = __fadd_rn(acc, widen(src[j][i]));
+    for (int j = 1; j < p; ++j) {
+      acc = __fadd_rn(acc, widen(src[j][i]));
+      if constexpr (HOP) acc = round_bf16(acc);
+    }
     const T y = narrow<T>(__fdiv_rn(acc, a.divisor));
     if (a.scatter) {
       sdst[i - lo] = y;
@@ -79,7 +82,10 @@ __global__ void __launch_bounds__(kThreads) k_fused_reduce_ldst(const __grid_con
         float t[V];
         Vec<T>::unpack(x[j], t);
 #pragma unroll
-        for (int l = 0; l < V; ++l) acc[l] = __fadd_rn(acc[l], t[l]);
+        for (int l = 0; l < V; ++l) {
+          acc[l] = __fadd_rn(acc[l], t[l]);
+          if constexpr (HOP) acc[l] = round_bf16(acc[l]);
+        }
       }
     } else {
       constexpr int B = 8;
@@ -100,7 +106,10 @@ __global__ void __launch_bounds__(kThreads) k_fused_reduce_ldst(const __grid_con
               for (int l = 0; l < V; ++l) acc[l] = t[l];
             } else {
 #pragma unroll
-              for (int l = 0; l < V; ++l) acc[l] = __fadd_rn(acc[l], t[l]);
+              for (int l = 0; l < V; ++l) {
+                acc[l] = __fadd_rn(acc[l], t[l]);
+                if constexpr (HOP) acc[l] = round_bf16(acc[l]);
+              }
             }
           }
         }
@@ -214,39 +223,66 @@ __device__ __forceinline__ void staged_scalar(const StagedArgs& a, int c, int64_
   }
 }
 
+constexpr int kConsumerWarps = 8;
+constexpr int kStagedThreads = 32 * (1 + kConsumerWarps);  // warp 0 produces, warps 1.. consume
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumerWarps) : "memory");
+}
+
+// Warp-specialised pipeline over S stages of p tile slots each.
+//   producer (warp 0, one lane): for its j-th tile, waits until stage j % S
+//     is released, then loads the p replicas' tiles into it (bulk copies that
+//     complete on full[st]);
+//   consumers (warps 1..8): wait on full[st], fold the p slots in ring order
+//     and write the result over slot 0 (each thread only touches the vectors
+//     it read); after a consumer-only barrier one consumer thread issues the
+//     p bulk stores of slot 0 and, once the previous tile's stores have read
+//     their shared memory, releases that tile's stage (empty[st]).
+// Every wait is bounded; on a timeout the CTA records the error and stops.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) k_fused_reduce_staged(const __grid_constant__ StagedArgs a) {
+__global__ void __launch_bounds__(kStagedThreads, 1) k_fused_reduce_staged(const __grid_constant__ StagedArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int V = Vec<T>::N;
   const int p = a.p;
   const int S = a.stages;
   const int tile_bytes = a.tile_elems * static_cast<int>(sizeof(T));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  unsigned char* data = smem + 128;                        // [S][p][tile_bytes]
-  unsigned char* res = data + static_cast<size_t>(S) * p * tile_bytes;  // [S][tile_bytes]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  unsigned char* data = smem + 128;  // [S][p][tile_bytes]
   __shared__ int s_abort;
+  const int warp = threadIdx.x / 32;
+  const int ctid = threadIdx.x - 32;  // consumer thread index (valid for warp >= 1)
 
-  // 1. elements outside the aligned bodies, scalar, chunks round-robin over CTAs
-  for (int c = blockIdx.x; c < p; c += gridDim.x) {
-    const int64_t lo = min(a.n, static_cast<int64_t>(c) * a.cs);
-    const int64_t hi = min(a.n, lo + a.cs);
-    const int64_t b0 = a.body_lo[c], b1 = a.body_lo[c] + a.body_len[c];
-    for (int64_t i = lo + threadIdx.x; i < b0; i += blockDim.x) staged_scalar<T>(a, c, i);
-    for (int64_t i = b1 + threadIdx.x; i < hi; i += blockDim.x) staged_scalar<T>(a, c, i);
+  // 1. elements outside the aligned bodies: consumers, chunks round-robin over CTAs
+  if (warp >= 1) {
+    for (int c = blockIdx.x; c < p; c += gridDim.x) {
+      const int64_t lo = min(a.n, static_cast<int64_t>(c) * a.cs);
+      const int64_t hi = min(a.n, lo + a.cs);
+      const int64_t b0 = a.body_lo[c], b1 = a.body_lo[c] + a.body_len[c];
+      for (int64_t i = lo + ctid; i < b0; i += 32 * kConsumerWarps) staged_scalar<T>(a, c, i);
+      for (int64_t i = b1 + ctid; i < hi; i += 32 * kConsumerWarps) staged_scalar<T>(a, c, i);
+    }
   }
 
-  // 2. the aligned bodies, tile by tile
   const int32_t total = a.tile0[p];
-  const int my_tiles = (blockIdx.x < total) ? (total - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+  const int my_tiles = (static_cast<int32_t>(blockIdx.x) < total)
+                           ? (total - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                           : 0;
   if (my_tiles == 0) return;
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int st = 0; st < S; ++st) mbar_init(smem_addr(&bars[st]), 1);
+    for (int st = 0; st < S; ++st) {
+      mbar_init(smem_addr(&full[st]), 1);
+      mbar_init(smem_addr(&empty[st]), 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
-  // tile geometry: chunk, first element, element count
   auto tile_at = [&](int j, int& c, int64_t& i0, int& len) {
     const int32_t g = static_cast<int32_t>(blockIdx.x) + j * static_cast<int32_t>(gridDim.x);
     int lo = 0, hi = p;  // tile0[lo] <= g < tile0[hi]
@@ -259,44 +295,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_reduce_staged(const __gri
     i0 = a.body_lo[c] + off;
     len = static_cast<int>(min(static_cast<int64_t>(a.tile_elems), a.body_len[c] - off));
   };
-  auto issue_loads = [&](int j, int st) {
-    int c, len;
-    int64_t i0;
-    tile_at(j, c, i0, len);
-    const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
-    const uint32_t bar = smem_addr(&bars[st]);
-    mbar_arrive_expect_tx(bar, bytes * p);
-    for (int r = 0; r < p; ++r)
-      bulk_load(smem_addr(data + (static_cast<size_t>(st) * p + r) * tile_bytes),
-                reinterpret_cast<const T*>(a.rep[r]) + i0, bytes, bar);
-  };
 
-  if (threadIdx.x == 0)
-    for (int j = 0; j < S && j < my_tiles; ++j) issue_loads(j, j);
+  if (warp == 0) {
+    if (threadIdx.x == 0) {
+      for (int j = 0; j < my_tiles; ++j) {
+        const int st = j % S;
+        if (j >= S) {
+          const uint32_t parity = static_cast<uint32_t>(j / S - 1) & 1u;
+          if (!mbar_wait_bounded(smem_addr(&empty[st]), parity, a.timeout_ns)) {
+            atomicCAS(&g_device_error, 0, kErrBulkWait);
+            atomicExch(&s_abort, 1);
+            break;
+          }
+        }
+        if (atomicAdd(&s_abort, 0)) break;
+        int c, len;
+        int64_t i0;
+        tile_at(j, c, i0, len);
+        const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
+        const uint32_t bar = smem_addr(&full[st]);
+        mbar_arrive_expect_tx(bar, bytes * p);
+        for (int r = 0; r < p; ++r)
+          bulk_load(smem_addr(data + (static_cast<size_t>(st) * p + r) * tile_bytes),
+                    reinterpret_cast<const T*>(a.rep[r]) + i0, bytes, bar);
+      }
+    }
+    return;
+  }
 
+  // consumers
+  const bool issuer = (ctid == 0);
   int j = 0;
   for (; j < my_tiles; ++j) {
     const int st = j % S;
     const uint32_t parity = static_cast<uint32_t>(j / S) & 1u;
-    if (threadIdx.x == 0) {
-      bulk_wait_read(S - 1);  // the stores that last read res[st] are done with it
-      if (!mbar_wait_bounded(smem_addr(&bars[st]), parity, a.timeout_ns)) {
-        atomicCAS(&g_device_error, 0, kErrBulkWait);
-        s_abort = 1;
-      }
+    bool ok = mbar_wait_bounded(smem_addr(&full[st]), parity, a.timeout_ns);
+    if (!ok) {
+      atomicCAS(&g_device_error, 0, kErrBulkWait);
+      atomicExch(&s_abort, 1);
     }
-    __syncthreads();
-    if (s_abort) break;
-    (void)mbar_try_wait(smem_addr(&bars[st]), parity);  // completed: acquire for this thread
-
+    consumers_sync();
+    if (atomicAdd(&s_abort, 0)) break;
     int c, len;
     int64_t i0;
     tile_at(j, c, i0, len);
     const int o = (c + a.shift) % p;
-    const unsigned char* stage = data + static_cast<size_t>(st) * p * tile_bytes;
-    unsigned char* out = res + static_cast<size_t>(st) * tile_bytes;
+    unsigned char* stage = data + static_cast<size_t>(st) * p * tile_bytes;
     const int nvec = len / V;
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    for (int v = ctid; v < nvec; v += 32 * kConsumerWarps) {
       float acc[V];
       Vec<T>::unpack(*reinterpret_cast<const uint4*>(stage + static_cast<size_t>(o) * tile_bytes + v * 16), acc);
       int r = o;
@@ -309,29 +355,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_reduce_staged(const __gri
       }
 #pragma unroll
       for (int l = 0; l < V; ++l) acc[l] = __fdiv_rn(acc[l], a.divisor);
-      *reinterpret_cast<uint4*>(out + v * 16) = Vec<T>::pack(acc);
+      *reinterpret_cast<uint4*>(stage + v * 16) = Vec<T>::pack(acc);  // over slot 0
     }
     fence_proxy_async_smem();
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    consumers_sync();
+    if (issuer) {
       const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
+      const uint32_t src = smem_addr(stage);
       if (a.scatter) {
         T* d = reinterpret_cast<T*>(a.out[(o + p - 1) % p]) + (i0 - static_cast<int64_t>(c) * a.cs);
-        bulk_store(d, smem_addr(out), bytes);
+        bulk_store(d, src, bytes);
       } else {
-        for (int r = 0; r < p; ++r) bulk_store(reinterpret_cast<T*>(a.rep[r]) + i0, smem_addr(out), bytes);
+        for (int r = 0; r < p; ++r) bulk_store(reinterpret_cast<T*>(a.rep[r]) + i0, src, bytes);
       }
       bulk_commit();
-      if (j + S < my_tiles) issue_loads(j + S, st);
+      if (j >= 1) {  // the previous tile's stores have read their stage: release it
+        bulk_wait_read(1);
+        mbar_arrive(smem_addr(&empty[(j - 1) % S]));
+      }
     }
   }
-
-  if (threadIdx.x == 0) {
-    bulk_wait_all();
-    if (s_abort) {  // let the loads still in flight land before the CTA's shared memory goes away
-      for (int k = j + 1; k < my_tiles && k < j + S; ++k)
-        (void)mbar_wait_bounded(smem_addr(&bars[k % S]), static_cast<uint32_t>(k / S) & 1u, a.timeout_ns);
-    }
+  if (issuer) bulk_wait_all();
+  if (atomicAdd(&s_abort, 0) && issuer) {
+    // let loads still in flight land before the CTA's shared memory goes away
+    for (int k = j + 1; k < my_tiles && k < j + S; ++k)
+      (void)mbar_wait_bounded(smem_addr(&full[k % S]), static_cast<uint32_t>(k / S) & 1u, a.timeout_ns);
   }
 }
 
@@ -410,12 +458,107 @@ __global__ void __launch_bounds__(kThreads) k_rs_step_ws(const __grid_constant__
     for (int q = 0; q < kU; ++q) {
       const int64_t e = base + q * kThreads + threadIdx.x;
       if (e < len) {
-        const float v = __fadd_rn(part[q], loc[q]);
+        float v = __fadd_rn(part[q], loc[q]);
+        if (a.hop_round) v = round_bf16(v);
         if (a.last) od[e] = narrow<T>(__fdiv_rn(v, a.divisor));
         else wcur[e] = v;
       }
     }
   }
+}
+
+
+// ------------------------------------------- persistent literal ring (fp32)
+// The literal 2(p-1)-step schedule in one cooperative launch ("Collective Ops
+// From Scratch", "Ring allreduce in two passes": each rank receives one chunk
+// per step from its left neighbour; its exercise of a configurable receive
+// timeout that surfaces a deadline error). Receiver d at step t needs the
+// chunk its sender d-1 finished at step t-1, so it waits until the sender has
+// posted t steps; every other ordering follows from that chain. Waits are
+// bounded by %globaltimer; a wait that runs out records where it gave up and
+// the block stops, so its own successors time out after it and the kernel
+// ends. Data of other ranks is read through L2 (ld.global.cg): L1 is not
+// coherent across SMs.
+constexpr int kErrRingWait = 2;  // device error code: a ring step's wait ran out
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads) k_ring_persistent_f32(const __grid_constant__ PersistArgs a) {
+  const int B = a.blocks_per_rank, p = a.p;
+  const int r = blockIdx.x / B, b = blockIdx.x % B;
+  const int snd = (r + p - 1) % p;  // this rank's left neighbour
+  const int T = 2 * (p - 1);
+  float* mine = reinterpret_cast<float*>(a.buf[r]);
+  const float* theirs = reinterpret_cast<const float*>(a.buf[snd]);
+  __shared__ int s_ok;
+  // Bounded wait until the sender has posted `need` steps; on a timeout record
+  // (rank, need) and return false.
+  auto wait_sender = [&](int need) -> bool {
+    if (threadIdx.x == 0) {
+      const int* f = a.flags + snd * B + b;
+      int ok = 1;
+      if (ld_acquire_gpu(f) < need) {
+        const uint64_t t0 = global_ns();
+        while (ld_acquire_gpu(f) < need) {
+          if (static_cast<int64_t>(global_ns() - t0) > a.timeout_ns) {
+            ok = 0;
+            break;
+          }
+          __nanosleep(256);
+        }
+      }
+      if (!ok) {
+        if (a.status) {
+          if (atomicCAS(&a.status[0], 0, static_cast<int>(DDP_ERR_TIMEOUT)) == 0) {
+            a.status[1] = r;
+            a.status[2] = need;
+          }
+          atomicAdd(&a.status[3], 1);
+        }
+        atomicCAS(&g_device_error, 0, kErrRingWait);
+      }
+      s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+  };
+  for (int t = 0; t < T; ++t) {
+    if (r == a.fault_rank && t == a.fault_step) return;  // injected fault: never posts step t
+    if (t > 0 && !wait_sender(t)) return;
+    const bool rs = t < p - 1;
+    const int c = rs ? ((snd - t) % p + p) % p : ((snd + 1 - (t - (p - 1))) % p + p) % p;
+    const int64_t lo = min(a.n, static_cast<int64_t>(c) * a.cs);
+    const int64_t hi = min(a.n, lo + a.cs);
+    const int64_t span = (hi - lo + B - 1) / B;
+    const int64_t x0 = min(hi, lo + static_cast<int64_t>(b) * span);
+    const int64_t x1 = min(hi, x0 + span);
+    const bool last_rs = (t == p - 2);
+    for (int64_t i = x0 + threadIdx.x; i < x1; i += blockDim.x) {
+      const float recv = __ldcg(theirs + i);
+      if (rs) {
+        float y = __fadd_rn(mine[i], recv);
+        if (last_rs) y = __fdiv_rn(y, a.divisor);
+        mine[i] = y;
+      } else {
+        mine[i] = recv;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      st_release_gpu(a.flags + r * B + b, t + 1);
+    }
+  }
+  // The sender's last step is read by no later step: wait for it too, so a
+  // rank that stops before its final step is still caught.
+  (void)wait_sender(T);
 }
 
 // ------------------------------------------------------------- launchers
@@ -433,16 +576,16 @@ int blocks_per_chunk(int64_t work_items, int per_block, int chunks) {
   return static_cast<int>(bx);
 }
 
-template <typename T>
+template <typename T, bool HOP>
 cudaError_t fused_ldst(const FusedArgs& a, cudaStream_t s) {
   constexpr int V = Vec<T>::N;
   const dim3 grid(blocks_per_chunk(a.cs / V + 1, kThreads, a.p), a.p);
   switch (a.p) {
-    case 2: k_fused_reduce_ldst<T, 2><<<grid, kThreads, 0, s>>>(a); break;
-    case 4: k_fused_reduce_ldst<T, 4><<<grid, kThreads, 0, s>>>(a); break;
-    case 8: k_fused_reduce_ldst<T, 8><<<grid, kThreads, 0, s>>>(a); break;
-    case 16: k_fused_reduce_ldst<T, 16><<<grid, kThreads, 0, s>>>(a); break;
-    default: k_fused_reduce_ldst<T, 0><<<grid, kThreads, 0, s>>>(a); break;
+    case 2: k_fused_reduce_ldst<T, 2, HOP><<<grid, kThreads, 0, s>>>(a); break;
+    case 4: k_fused_reduce_ldst<T, 4, HOP><<<grid, kThreads, 0, s>>>(a); break;
+    case 8: k_fused_reduce_ldst<T, 8, HOP><<<grid, kThreads, 0, s>>>(a); break;
+    case 16: k_fused_reduce_ldst<T, 16, HOP><<<grid, kThreads, 0, s>>>(a); break;
+    default: k_fused_reduce_ldst<T, 0, HOP><<<grid, kThreads, 0, s>>>(a); break;
   }
   count_launch();
   return cudaGetLastError();
@@ -474,13 +617,13 @@ template <typename T>
 bool plan_staged(const FusedArgs& f, StagedArgs& a) {
   constexpr int V = Vec<T>::N;
   const int p = f.p;
-  if (p > kMaxStagedP || !f.same_align) return false;
+  if (p > kMaxStagedP || !f.same_align || f.hop_round) return false;
   const uintptr_t base = reinterpret_cast<uintptr_t>(f.src[0]);
   if (base % sizeof(T) != 0) return false;
   std::memset(&a, 0, sizeof(a));
   int tile_bytes = 16384;
-  while (tile_bytes > 512 && static_cast<int64_t>(p + 1) * tile_bytes * 3 > kStagedSmemBudget) tile_bytes /= 2;
-  int stages = static_cast<int>(kStagedSmemBudget / (static_cast<int64_t>(p + 1) * tile_bytes));
+  while (tile_bytes > 512 && static_cast<int64_t>(p) * tile_bytes * 4 > kStagedSmemBudget) tile_bytes /= 2;
+  int stages = static_cast<int>(kStagedSmemBudget / (static_cast<int64_t>(p) * tile_bytes));
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return false;
   a.tile_elems = tile_bytes / static_cast<int>(sizeof(T));
@@ -516,7 +659,7 @@ bool plan_staged(const FusedArgs& f, StagedArgs& a) {
 
 template <typename T>
 cudaError_t fused_staged(const StagedArgs& a, cudaStream_t s) {
-  const size_t smem = 128 + static_cast<size_t>(a.stages) * (a.p + 1) * a.tile_elems * sizeof(T);
+  const size_t smem = 128 + static_cast<size_t>(a.stages) * a.p * a.tile_elems * sizeof(T);
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -529,7 +672,7 @@ cudaError_t fused_staged(const StagedArgs& a, cudaStream_t s) {
   int grid = sm_count();
   if (a.tile0[a.p] < grid) grid = a.tile0[a.p] > a.p ? a.tile0[a.p] : a.p;
   if (grid < 1) grid = 1;
-  k_fused_reduce_staged<T><<<grid, kThreads, smem, s>>>(a);
+  k_fused_reduce_staged<T><<<grid, kStagedThreads, smem, s>>>(a);
   count_launch();
   return cudaGetLastError();
 }
@@ -541,7 +684,8 @@ cudaError_t launch_fused_reduce(const FusedArgs& a, ddp_dtype dt, bool staged, c
     if (dt == DDP_FLOAT32 ? plan_staged<float>(a, sa) : plan_staged<__nv_bfloat16>(a, sa))
       return dt == DDP_FLOAT32 ? fused_staged<float>(sa, s) : fused_staged<__nv_bfloat16>(sa, s);
   }
-  return dt == DDP_FLOAT32 ? fused_ldst<float>(a, s) : fused_ldst<__nv_bfloat16>(a, s);
+  if (dt == DDP_FLOAT32) return fused_ldst<float, false>(a, s);
+  return a.hop_round ? fused_ldst<__nv_bfloat16, true>(a, s) : fused_ldst<__nv_bfloat16, false>(a, s);
 }
 
 cudaError_t launch_rs_step_inplace_f32(const RingStepArgs& a, cudaStream_t s) {
@@ -557,6 +701,21 @@ cudaError_t launch_rs_step_ws(const RingStepArgs& a, ddp_dtype dt, cudaStream_t 
   else k_rs_step_ws<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a);
   count_launch();
   return cudaGetLastError();
+}
+
+int ring_persistent_max_blocks() {
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_ring_persistent_f32, kThreads, 0) != cudaSuccess)
+    return 0;
+  return blocks * sm_count();
+}
+
+cudaError_t launch_ring_persistent(const PersistArgs& a, cudaStream_t s) {
+  void* args[] = {const_cast<PersistArgs*>(&a)};
+  const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_ring_persistent_f32),
+                                                    dim3(a.p * a.blocks_per_rank), dim3(kThreads), args, 0, s);
+  count_launch();
+  return e;
 }
 
 cudaError_t read_device_error(cudaStream_t s, int* code) {

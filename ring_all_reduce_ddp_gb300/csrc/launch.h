@@ -14,6 +14,10 @@ cudaError_t launch_fused_reduce(const FusedArgs& a, ddp_dtype dt, bool staged, c
 cudaError_t launch_rs_step_inplace_f32(const RingStepArgs& a, cudaStream_t s);
 cudaError_t launch_rs_step_ws(const RingStepArgs& a, ddp_dtype dt, cudaStream_t s);
 cudaError_t launch_bucket_allreduce(const BucketArgs& a, ddp_dtype dt, cudaStream_t s);
+cudaError_t launch_bucket_table(const BucketTable& t, int32_t total_tiles, float divisor, ddp_dtype dt,
+                                cudaStream_t s);
+cudaError_t launch_ring_persistent(const PersistArgs& a, cudaStream_t s);
+int ring_persistent_max_blocks();  // co-resident blocks of the persistent ring kernel on this device
 cudaError_t launch_pair_copy(const PairCopyArgs& a, cudaStream_t s);
 cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s);
 cudaError_t launch_seg_copy(const SegCopyArgs& a, ddp_dtype dt, cudaStream_t s);

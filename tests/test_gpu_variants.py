@@ -1,0 +1,71 @@
+"""GPU parity of the variants beyond the default path: the per-hop bf16 ring
+(partials rounded to bf16 at every hop, as a bf16 wire format carries them),
+in its literal and fused forms, against the oracle's per-hop simulation."""
+import numpy as np
+import pytest
+
+import ring_all_reduce_ddp_gb300 as D
+from oracle import ring as orc
+from oracle.bf16 import bf16_to_f32, f32_to_bf16
+from tests.helpers import assert_bit_equal, make_replicas, to_host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ALGOS = [D.DDP_ALGO_FUSED, D.DDP_ALGO_FUSED_LDST, D.DDP_ALGO_FUSED_TMA, D.DDP_ALGO_RING_STEPS]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("p,n", [(1, 100), (2, 4099), (3, 10007), (8, 65536 * 3 + 5), (16, 100003), (17, 5001),
+                                 (64, 262147)])
+def test_per_hop_bf16_matches_oracle(p, n, algo):
+    devs, hosts, _ = make_replicas(p, n, "bf16", "normal", seed=700 + p)
+    D.ddp_allreduce_ex(devs, n, D.DDP_BFLOAT16, float(p), algo, D.DDP_FLAG_ROUND_EACH_HOP)
+    want, _ = orc.allreduce(hosts, n, float(p), "bf16", hop_round=True)
+    for r in range(p):
+        assert_bit_equal(to_host(devs[r]), want[r], f"replica {r}")
+    assert D.ddp_device_error() == 0
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_per_hop_worked_example(algo):
+    """256 on each chunk's origin rank, 1 elsewhere, p = 8: per hop 256, accumulated 264."""
+    p, n = 8, 8 * 1000
+    cs = n // p
+    hop, acc = [], []
+    for r in range(p):
+        v = np.ones(n, dtype=np.float32)
+        v[r * cs:(r + 1) * cs] = 256.0
+        b = torch.from_numpy(f32_to_bf16(v).view(np.int16)).view(torch.bfloat16).cuda()
+        hop.append(b)
+        acc.append(b.clone())
+    D.ddp_allreduce_ex(hop, n, D.DDP_BFLOAT16, 1.0, algo, D.DDP_FLAG_ROUND_EACH_HOP)
+    D.ddp_allreduce(acc, n, D.DDP_BFLOAT16, 1.0, algo)
+    assert np.all(bf16_to_f32(to_host(hop[0])) == 256.0)
+    assert np.all(bf16_to_f32(to_host(acc[0])) == 264.0)
+
+
+def test_per_hop_error_grows_with_p_on_the_gpu():
+    """Mean |error| against the exact sum: rounding every hop versus once."""
+    n = 1 << 18
+    ratio = {}
+    for p in (2, 8, 32):
+        a, hosts, _ = make_replicas(p, n, "bf16", "normal", seed=800 + p)
+        b = [t.clone() for t in a]
+        D.ddp_allreduce_ex(a, n, D.DDP_BFLOAT16, 1.0, D.DDP_ALGO_FUSED, 0)
+        D.ddp_allreduce_ex(b, n, D.DDP_BFLOAT16, 1.0, D.DDP_ALGO_FUSED, D.DDP_FLAG_ROUND_EACH_HOP)
+        exact = np.sum(np.stack([bf16_to_f32(h) for h in hosts]).astype(np.float64), axis=0)
+        e_once = np.mean(np.abs(bf16_to_f32(to_host(a[0])) - exact))
+        e_hop = np.mean(np.abs(bf16_to_f32(to_host(b[0])) - exact))
+        ratio[p] = e_hop / e_once
+    assert ratio[2] >= 1.0 and ratio[8] > 1.5 and ratio[32] > ratio[8]
+
+
+def test_per_hop_flag_needs_bf16():
+    devs, _, _ = make_replicas(2, 100, "f32")
+    with pytest.raises(D.DDPError) as e:
+        D.ddp_allreduce_ex(devs, 100, D.DDP_FLOAT32, 1.0, D.DDP_ALGO_FUSED, D.DDP_FLAG_ROUND_EACH_HOP)
+    assert e.value.status == D.DDP_ERR_DTYPE
+    with pytest.raises(D.DDPError) as e:
+        D.ddp_allreduce_ex(devs, 100, D.DDP_FLOAT32, 1.0, D.DDP_ALGO_FUSED, 8)
+    assert e.value.status == D.DDP_ERR_ARG
