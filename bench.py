@@ -456,7 +456,7 @@ def run_sweep(args, ranks: Ranks):
     ps = [int(x) for x in os.environ.get("SWEEP_P", "2,4,8,16,64").split(",")]
     max_k = int(os.environ.get("SWEEP_MAX_K", "10"))
     ops = os.environ.get("SWEEP_OPS", "allreduce,reduce_scatter_rank,reduce_scatter_ring,allgather,broadcast")
-    algos = os.environ.get("SWEEP_ALGOS", "fused,ring_steps").split(",")
+    algos = os.environ.get("SWEEP_ALGOS", "fused,ring_steps,persistent").split(",")
     reps = int(os.environ.get("SWEEP_REPS", "20"))
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
@@ -476,8 +476,13 @@ def run_sweep(args, ranks: Ranks):
                 if ops != "allreduce" else []
             for op in ops.split(","):
                 for an in algos:
-                    al = algo_code(an)
-                    if op == "allreduce":
+                    if an == "persistent" and op != "allreduce":
+                        continue
+                    al = algo_code(an) if an != "persistent" else None
+                    if op == "allreduce" and an == "persistent":
+                        fn = lambda: D.ddp_allreduce_persistent(bufs, n, D.DDP_FLOAT32, float(p))
+                        nbytes = 2 * p * M
+                    elif op == "allreduce":
                         fn = lambda: D.ddp_allreduce(bufs, n, D.DDP_FLOAT32, float(p), al)
                         nbytes = 2 * p * M
                     elif op.startswith("reduce_scatter"):
