@@ -328,33 +328,62 @@ def run_ours(args, ranks: Ranks):
                    "in one launch" if mode == D.DDP_SYNC_IN_PLACE
                    else "flatten, fused all-reduce, unflatten per bucket (whole sync timed)")
 
-    # End to end through the public API: every replica's gradients in from pinned
-    # host memory, one step, the synchronised gradients out, every step.
+    # End to end through the public API: every step copies every replica's
+    # gradients in from pinned host memory, synchronises them and copies the
+    # result out. Two device copies of the workload alternate so that step i's
+    # copy-out (D2H stream) overlaps step i+1's copy-in (H2D stream); the sync
+    # runs on the compute stream between them.
+    grads_b, arenas_b = W.make_grads(cfg, f"cuda:{dev}")
+    red_b = Reducer(grads_b, cfg["first_cap"], cfg["cap"])
+    sets = [(arenas, red), (arenas_b, red_b)]
     host_in = [a.detach().to("cpu").pin_memory() for a in arenas]
     host_out = [torch.empty_like(h).pin_memory() for h in host_in]
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [None, None]
 
-    def e2e_step():
-        for a, h in zip(arenas, host_in):
-            a.copy_(h, non_blocking=True)
-        step()
-        for a, h in zip(arenas, host_out):
-            h.copy_(a, non_blocking=True)
+    def e2e_step(i):
+        k = i % 2
+        ar_k, red_k = sets[k]
+        with torch.cuda.stream(h2d_s):
+            if d2h_done[k] is not None:
+                h2d_s.wait_event(d2h_done[k])  # this set's previous result has been read out
+            for a, h in zip(ar_k, host_in):
+                a.copy_(h, non_blocking=True)
+            h2d_done[k].record(h2d_s)
+        stream.wait_event(h2d_done[k])
+        if not red_k.assign():
+            raise RuntimeError("bucket assignment changed")
+        if bsync:
+            bsync(bc_algo, stream)
+        red_k.sync_gradients(divisor, algo, mode, 1.0, stream)
+        comp_done[k].record(stream)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(comp_done[k])
+            for a, h in zip(ar_k, host_out):
+                h.copy_(a, non_blocking=True)
+            d2h_done[k] = torch.cuda.Event()
+            d2h_done[k].record(d2h_s)
 
-    for _ in range(min(3, max(args.warmup, 1))):
-        e2e_step()
+    for i in range(max(4, min(args.warmup, 8))):
+        e2e_step(i)
     torch.cuda.synchronize()
     ranks.barrier()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    f0.record(h2d_s)
+    stream.wait_stream(h2d_s)
+    for i in range(args.steps):
+        e2e_step(i)
+    stream.wait_stream(d2h_s)
     f1.record(stream)
     torch.cuda.synchronize()
     ranks.barrier()
     e2e_ms = ranks.max(f0.elapsed_time(f1))
     io = sum(a.numel() * a.element_size() for a in arenas)
     e2e = {"value": round(step_bytes * args.steps * ranks.world / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
-           "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "ms_per_step": round(e2e_ms / args.steps, 4)}
+           "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "ms_per_step": round(e2e_ms / args.steps, 4),
+           "pipeline": "step i's copy-out overlaps step i+1's copy-in (two device copies, three streams)"}
+    del red_b, grads_b, arenas_b
 
     # the three-kernel form of the same step, for comparison (not the headline)
     other = None
@@ -456,7 +485,8 @@ def run_sweep(args, ranks: Ranks):
     ps = [int(x) for x in os.environ.get("SWEEP_P", "2,4,8,16,64").split(",")]
     max_k = int(os.environ.get("SWEEP_MAX_K", "10"))
     ops = os.environ.get("SWEEP_OPS", "allreduce,reduce_scatter_rank,reduce_scatter_ring,allgather,broadcast")
-    algos = os.environ.get("SWEEP_ALGOS", "fused,ring_steps,persistent").split(",")
+    algos = os.environ.get("SWEEP_ALGOS", "fused,ring_steps,persistent,rd,rab,tree").split(",")
+    tree_codes = {"rd": D.DDP_ALGO_RECURSIVE_DOUBLING, "rab": D.DDP_ALGO_RABENSEIFNER, "tree": D.DDP_ALGO_TREE}
     reps = int(os.environ.get("SWEEP_REPS", "20"))
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
@@ -476,9 +506,9 @@ def run_sweep(args, ranks: Ranks):
                 if ops != "allreduce" else []
             for op in ops.split(","):
                 for an in algos:
-                    if an == "persistent" and op != "allreduce":
+                    if an in ("persistent", "rd", "rab", "tree") and op != "allreduce":
                         continue
-                    al = algo_code(an) if an != "persistent" else None
+                    al = tree_codes[an] if an in tree_codes else (algo_code(an) if an != "persistent" else None)
                     if op == "allreduce" and an == "persistent":
                         fn = lambda: D.ddp_allreduce_persistent(bufs, n, D.DDP_FLOAT32, float(p))
                         nbytes = 2 * p * M

@@ -63,9 +63,17 @@ typedef enum {
                                library picks its fastest one-pass kernel             */
   DDP_ALGO_RING_STEPS = 1,  /* the literal schedule: one launch per ring step         */
   DDP_ALGO_FUSED_LDST = 2,  /* one pass through registers (128-bit loads and stores) */
-  DDP_ALGO_FUSED_TMA = 3    /* one pass staged through shared memory by bulk
+  DDP_ALGO_FUSED_TMA = 3,   /* one pass staged through shared memory by bulk
                                asynchronous copies (falls back to the register path
                                when p > 64 or the replicas' alignments differ)      */
+  /* Tree-shaped literal all-reduces ([DP] "Latency, trees, and choosing an
+   * algorithm"; [COLL] tree all-reduce). ddp_allreduce only; fp32 only
+   * (DDP_ERR_DTYPE otherwise); the pairwise tree order, not the ring's. */
+  DDP_ALGO_RECURSIVE_DOUBLING = 4, /* log2 p steps: pairs r, r^2^j swap and add; p = 2^k */
+  DDP_ALGO_RABENSEIFNER = 5,       /* recursive halving (keep lower half if bit d clear),
+                                      then recursive doubling of owned chunks; p = 2^k */
+  DDP_ALGO_TREE = 6                /* binomial reduce to rank 0, divide there, then the
+                                      doubling-tree broadcast; any p                  */
 } ddp_algo;
 
 typedef enum {

@@ -25,6 +25,7 @@ DDP_ERR_NOMEM, DDP_ERR_CUDA, DDP_ERR_TIMEOUT, DDP_ERR_STATE = 5, 6, 7, 8
 DDP_FLOAT32, DDP_BFLOAT16 = 0, 1
 # ddp_algo
 DDP_ALGO_FUSED, DDP_ALGO_RING_STEPS, DDP_ALGO_FUSED_LDST, DDP_ALGO_FUSED_TMA = 0, 1, 2, 3
+DDP_ALGO_RECURSIVE_DOUBLING, DDP_ALGO_RABENSEIFNER, DDP_ALGO_TREE = 4, 5, 6
 # ddp_own
 DDP_OWN_RANK, DDP_OWN_RING = 0, 1
 # ddp_border

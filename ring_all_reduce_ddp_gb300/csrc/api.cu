@@ -273,7 +273,98 @@ ddp_status run_plan_once(Plan& pl, cudaStream_t s) {
 ddp_status check_algo(int algo) {
   DDP_CHECK(algo == DDP_ALGO_FUSED || algo == DDP_ALGO_RING_STEPS || algo == DDP_ALGO_FUSED_LDST ||
                 algo == DDP_ALGO_FUSED_TMA,
-            DDP_ERR_ARG, "unknown algo");
+            DDP_ERR_ARG, "unknown algo (the tree-shaped algos are for ddp_allreduce only)");
+  return DDP_OK;
+}
+
+bool is_tree_algo(int algo) {
+  return algo == DDP_ALGO_RECURSIVE_DOUBLING || algo == DDP_ALGO_RABENSEIFNER || algo == DDP_ALGO_TREE;
+}
+
+// The tree-shaped literal all-reduces, fp32 in place. See the oracle's
+// readings: recursive doubling pairs r, r ^ 2^j; Rabenseifner halves with
+// distance d = p / 2^(k+1), the rank with bit d clear keeping the lower half,
+// then doubles back; the tree reduces binomially to rank 0 and broadcasts.
+ddp_status run_tree_allreduce(float* const* B, int32_t p, int64_t n, float divisor, int algo, cudaStream_t s) {
+  auto pow2 = [](int32_t x) { return x >= 1 && (x & (x - 1)) == 0; };
+  if (algo != DDP_ALGO_TREE)
+    DDP_CHECK(pow2(p), DDP_ERR_ARG, "recursive doubling and Rabenseifner need p a power of two");
+  if (p == 1) return run_fused(reinterpret_cast<const void* const*>(B), reinterpret_cast<void* const*>(B), 1, n,
+                               DDP_FLOAT32, divisor, false, 0, false, s);
+  int L = 0;
+  while ((int64_t(1) << L) < p) ++L;
+  if (algo == DDP_ALGO_RECURSIVE_DOUBLING) {
+    for (int j = 0; j < L; ++j) {
+      const int d = 1 << j;
+      PairAddArgs a;
+      std::memset(&a, 0, sizeof(a));
+      for (int r = 0; r < p; ++r) {
+        if (r & d) continue;
+        const int k = a.njobs++;
+        a.a[k] = B[r]; a.b[k] = B[r | d]; a.d1[k] = B[r]; a.d2[k] = B[r | d];
+        a.lo[k] = 0; a.hi[k] = n;
+      }
+      a.divide = (j == L - 1); a.divisor = divisor;
+      DDP_CUDA(launch_pair_add(a, s), "recursive doubling step launch");
+    }
+    return DDP_OK;
+  }
+  if (algo == DDP_ALGO_RABENSEIFNER) {
+    const int64_t cs = chunk_size(n, p);
+    auto clip = [&](int64_t chunk) { return std::min(n, chunk * cs); };
+    for (int k = 0; k < L; ++k) {  // recursive halving
+      const int d = p >> (k + 1);
+      PairAddArgs a;
+      std::memset(&a, 0, sizeof(a));
+      for (int r = 0; r < p; ++r) {
+        if (r & d) continue;
+        const int64_t lo = r & ~(2 * d - 1);  // the pair's common segment, in chunks
+        const int q = r | d;
+        int j = a.njobs++;
+        a.a[j] = B[r]; a.b[j] = B[q]; a.d1[j] = B[r]; a.lo[j] = clip(lo); a.hi[j] = clip(lo + d);
+        j = a.njobs++;
+        a.a[j] = B[r]; a.b[j] = B[q]; a.d1[j] = B[q]; a.lo[j] = clip(lo + d); a.hi[j] = clip(lo + 2 * d);
+      }
+      a.divide = (k == L - 1); a.divisor = divisor;
+      DDP_CUDA(launch_pair_add(a, s), "recursive halving step launch");
+    }
+    for (int k = 0; k < L; ++k) {  // recursive doubling of the owned segments
+      const int d = 1 << k;
+      PairCopyArgs a;
+      std::memset(&a, 0, sizeof(a));
+      for (int r = 0; r < p; ++r) {
+        const int64_t lo = r & ~(d - 1);  // rank r's owned segment (d chunks)
+        a.src[r] = reinterpret_cast<const char*>(B[r] + clip(lo));
+        a.dst[r] = reinterpret_cast<char*>(B[r ^ d] + clip(lo));
+        a.nbytes[r] = (clip(lo + d) - clip(lo)) * 4;
+      }
+      a.njobs = p;
+      DDP_CUDA(launch_pair_copy(a, s), "recursive doubling copy launch");
+    }
+    return DDP_OK;
+  }
+  // tree: binomial reduce to rank 0, then the doubling-tree broadcast from rank 0
+  for (int64_t span = 1; span < p; span *= 2) {
+    PairAddArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int64_t r = 0; r + span < p; r += 2 * span) {
+      const int k = a.njobs++;
+      a.a[k] = B[r]; a.b[k] = B[r + span]; a.d1[k] = B[r]; a.lo[k] = 0; a.hi[k] = n;
+    }
+    a.divide = (2 * span >= p); a.divisor = divisor;
+    DDP_CUDA(launch_pair_add(a, s), "tree reduce step launch");
+  }
+  for (int64_t span = 1; span < p; span *= 2) {
+    PairCopyArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int64_t v = 0; v < span && v + span < p; ++v) {
+      const int k = a.njobs++;
+      a.src[k] = reinterpret_cast<const char*>(B[v]);
+      a.dst[k] = reinterpret_cast<char*>(B[v + span]);
+      a.nbytes[k] = n * 4;
+    }
+    DDP_CUDA(launch_pair_copy(a, s), "tree broadcast step launch");
+  }
   return DDP_OK;
 }
 
@@ -505,6 +596,19 @@ ddp_status ddp_bucket_unflatten(int32_t p, int32_t k, const void* const* bucket,
 
 ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
                          ddp_algo algo, cudaStream_t stream) {
+  if (is_tree_algo(algo)) {
+    DDP_TRY(check_common(p, n, dtype));
+    DDP_CHECK(dtype == DDP_FLOAT32, DDP_ERR_DTYPE, "the tree-shaped all-reduces run fp32 buffers");
+    DDP_TRY(check_divisor(divisor));
+    DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
+    std::vector<std::pair<uintptr_t, uintptr_t>> rg;
+    for (int r = 0; r < p; ++r) rg.push_back(range_of(bufs[r], n * 4));
+    DDP_CHECK(disjoint(rg), DDP_ERR_ARG, "replica buffers overlap");
+    if (n == 0) return DDP_OK;
+    std::vector<float*> B(p);
+    for (int r = 0; r < p; ++r) B[r] = static_cast<float*>(bufs[r]);
+    return run_tree_allreduce(B.data(), p, n, divisor, algo, stream);
+  }
   return ddp_allreduce_ex(bufs, p, n, dtype, divisor, algo, 0u, stream);
 }
 

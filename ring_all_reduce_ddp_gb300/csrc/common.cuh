@@ -160,6 +160,19 @@ struct PersistArgs {
   int64_t timeout_ns;          // bound of every wait
 };
 
+// Pair-add step of the tree-shaped all-reduces (fp32, in place): job j sets
+// y = a[j][i] + b[j][i] (then y / divisor if divide) for i in [lo[j], hi[j])
+// and stores y to d1[j][i] and, if d2[j] is set, to d2[j][i].
+struct PairAddArgs {
+  const float* a[kMaxP];
+  const float* b[kMaxP];
+  float* d1[kMaxP];
+  float* d2[kMaxP];
+  int64_t lo[kMaxP], hi[kMaxP];
+  int njobs, divide;
+  float divisor;
+};
+
 // Copy jobs: job j copies nbytes[j] bytes from src[j] to dst[j].
 struct PairCopyArgs {
   const char* src[kMaxP];

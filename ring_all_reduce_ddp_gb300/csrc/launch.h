@@ -19,6 +19,7 @@ cudaError_t launch_bucket_table(const BucketTable& t, int32_t total_tiles, float
 cudaError_t launch_ring_persistent(const PersistArgs& a, cudaStream_t s);
 int ring_persistent_max_blocks();  // co-resident blocks of the persistent ring kernel on this device
 cudaError_t launch_pair_copy(const PairCopyArgs& a, cudaStream_t s);
+cudaError_t launch_pair_add(const PairAddArgs& a, cudaStream_t s);
 cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s);
 cudaError_t launch_seg_copy(const SegCopyArgs& a, ddp_dtype dt, cudaStream_t s);
 cudaError_t launch_multi_fanout(const MultiFanoutArgs& a, cudaStream_t s);

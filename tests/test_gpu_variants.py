@@ -69,3 +69,50 @@ def test_per_hop_flag_needs_bf16():
     with pytest.raises(D.DDPError) as e:
         D.ddp_allreduce_ex(devs, 100, D.DDP_FLOAT32, 1.0, D.DDP_ALGO_FUSED, 8)
     assert e.value.status == D.DDP_ERR_ARG
+
+
+# ---------------------------------------------------------- tree-shaped all-reduces
+from oracle import trees as ot  # noqa: E402
+
+TREE = {"rd": (D.DDP_ALGO_RECURSIVE_DOUBLING, ot.recursive_doubling),
+        "rab": (D.DDP_ALGO_RABENSEIFNER, ot.rabenseifner),
+        "tree": (D.DDP_ALGO_TREE, ot.tree)}
+
+
+@pytest.mark.parametrize("name", ["rd", "rab"])
+@pytest.mark.parametrize("p,n", [(1, 100), (2, 1), (2, 4099), (4, 3), (4, 277421), (8, 65536 * 3 + 5), (16, 100003),
+                                 (64, 262147)])
+def test_power_of_two_trees_match_oracle(name, p, n):
+    algo, ref = TREE[name]
+    devs, hosts, _ = make_replicas(p, n, "f32", "normal", seed=1100 + p)
+    before = D.ddp_kernel_launches()
+    D.ddp_allreduce(devs, n, D.DDP_FLOAT32, float(p), algo)
+    launched = D.ddp_kernel_launches() - before
+    want, info = ref(hosts, n, float(p))
+    for r in range(p):
+        assert_bit_equal(to_host(devs[r]), want[r], f"replica {r}")
+    if p > 1:
+        assert launched == info["steps"]  # log2 p, or 2 log2 p for Rabenseifner
+
+
+@pytest.mark.parametrize("p,n", [(1, 10), (2, 4099), (3, 10007), (5, 3), (6, 65541), (8, 123457), (13, 50021),
+                                 (16, 100003)])
+def test_tree_matches_oracle(p, n):
+    algo, ref = TREE["tree"]
+    devs, hosts, _ = make_replicas(p, n, "f32", "uniform", seed=1200 + p)
+    D.ddp_allreduce(devs, n, D.DDP_FLOAT32, float(p), algo)
+    want, _ = ref(hosts, n, float(p))
+    for r in range(p):
+        assert_bit_equal(to_host(devs[r]), want[r], f"replica {r}")
+
+
+def test_tree_algos_reject_what_they_cannot_do():
+    devs, _, _ = make_replicas(6, 100, "f32")
+    for algo in (D.DDP_ALGO_RECURSIVE_DOUBLING, D.DDP_ALGO_RABENSEIFNER):
+        with pytest.raises(D.DDPError) as e:
+            D.ddp_allreduce(devs, 100, D.DDP_FLOAT32, 1.0, algo)
+        assert e.value.status == D.DDP_ERR_ARG
+    devs, _, _ = make_replicas(4, 100, "bf16")
+    with pytest.raises(D.DDPError) as e:
+        D.ddp_allreduce(devs, 100, D.DDP_BFLOAT16, 1.0, D.DDP_ALGO_TREE)
+    assert e.value.status == D.DDP_ERR_DTYPE
