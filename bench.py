@@ -66,6 +66,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--sweep", action="store_true", help="message-size / rank-count sweep, one line per point")
+    ap.add_argument("--overlap", action="store_true", help="exposed communication vs bucket cap, one line per cap")
     return ap.parse_args()
 
 
@@ -549,12 +550,103 @@ def run_sweep(args, ranks: Ranks):
             torch.cuda.empty_cache()
 
 
+# --------------------------------------------------------------- overlap
+def run_overlap(args, ranks: Ranks):
+    """Exposed communication against bucket cap, with readiness-driven firing.
+
+    A synthetic backward walks the parameters last-registered first on the
+    compute stream; each weight gradient costs two bf16 GEMMs with
+    4 * numel * n_tok FLOPs in all (backward is about 4N FLOPs per token);
+    after each gradient an event is recorded and the Reducer is told the
+    gradient is ready, which launches every newly complete bucket's in-place
+    all-reduce on a communication stream. For each cap: the backward alone,
+    backward + overlapped sync, and backward followed by the sync. One JSON
+    line per cap."""
+    import torch
+
+    import ring_all_reduce_ddp_gb300 as D
+    from ring_all_reduce_ddp_gb300 import build as B
+    from ring_all_reduce_ddp_gb300.reducer import Reducer
+    from synth import workloads as W
+    B.build_library()
+    if ranks.rank != 0:
+        return
+    torch.cuda.set_device(0)
+    cfg = W.CONFIGS[args.config]
+    grads, _ = W.make_grads(cfg, "cuda:0")
+    numel = W.numels(cfg)
+    k = len(numel)
+    divisor = W.divisor(cfg)
+    n_tok = int(os.environ.get("OVERLAP_TOKENS", "65536"))
+    kdim = 1024
+    x = torch.randn(n_tok, kdim, device="cuda", dtype=torch.bfloat16)
+    wmax = max((n + kdim - 1) // kdim for n in numel)
+    w = torch.randn(kdim, wmax, device="cuda", dtype=torch.bfloat16)
+    y = torch.empty(n_tok, wmax, device="cuda", dtype=torch.bfloat16)
+    compute = torch.cuda.current_stream()
+    comm = torch.cuda.Stream()
+
+    ready_events = [torch.cuda.Event() for _ in range(k)]
+
+    def backward(red=None):
+        for t in range(k - 1, -1, -1):
+            cols = (numel[t] + kdim - 1) // kdim
+            if numel[t] >= 4096:  # 2 GEMMs: 2 * (2 * n_tok * kdim * cols) ~ 4 * numel * n_tok FLOPs
+                torch.mm(x, w[:, :cols], out=y[:, :cols])
+                torch.mm(x, w[:, :cols], out=y[:, :cols])
+            if red is not None:
+                ready_events[t].record(compute)
+                red.mark_ready(t, divisor, ready_events[t], comm)
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(compute)
+        for _ in range(reps):
+            fn()
+        compute.wait_stream(comm)
+        b.record(compute)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    reps = max(5, min(args.steps, 50))
+    t_bwd = timed(lambda: backward(None), reps)
+    flops = 4.0 * sum(n for n in numel if n >= 4096) * n_tok
+    caps = [int(float(c) * (1 << 20)) for c in os.environ.get("OVERLAP_CAPS_MB", "0.25,1,5,25,100,100000").split(",")]
+    for cap in caps:
+        red = Reducer(grads, min(cfg["first_cap"], cap), cap)
+
+        def overlapped():
+            red.prepare()
+            backward(red)
+
+        def serial():
+            backward(None)
+            red.sync_gradients(divisor, D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE, 1.0, compute)
+
+        t_ov = timed(overlapped, reps)
+        t_se = timed(serial, reps)
+        t_comm = timed(lambda: red.sync_gradients(divisor, D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE, 1.0, compute), reps)
+        print(json.dumps({"overlap": args.config, "p": cfg["p"], "bucket_cap_mb": cap / (1 << 20),
+                          "buckets": len(red.buckets), "n_tok": n_tok,
+                          "backward_ms": round(t_bwd, 4), "backward_tflops": round(flops / (t_bwd / 1e3) / 1e12, 1),
+                          "sync_alone_ms": round(t_comm, 4), "overlapped_ms": round(t_ov, 4),
+                          "serial_ms": round(t_se, 4), "exposed_ms": round(t_ov - t_bwd, 4),
+                          "hidden_frac": (round(1 - (t_ov - t_bwd) / (t_se - t_bwd), 3)
+                                          if t_se - t_bwd > 0.05 * t_comm else None)}), flush=True)
+        red.destroy()
+
+
 def main():
     args = parse_args()
     ranks = Ranks()
     try:
         if args.sweep:
             run_sweep(args, ranks)
+        elif args.overlap:
+            run_overlap(args, ranks)
         elif args.impl == "reference":
             run_reference(args, ranks)
         else:

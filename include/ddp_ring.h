@@ -131,6 +131,18 @@ ddp_status ddp_bucket_assign(int32_t k, const int64_t* numel, int32_t elem_size,
                              int64_t* offset, int32_t* bucket_ptr, int32_t* bucket_tensors,
                              int64_t* bucket_numel);
 
+/* Bucket assignment along an explicit walk: the rebuild of [DDP] Part 2
+ * ("_rebuild_buckets": buckets rebuilt from the order in which gradients were
+ * observed to become ready). walk[k] is a permutation of 0..k-1, first-ready
+ * first; bucket 0 gets the first cap; a bucket closes once its bytes reach its
+ * cap; the list is not reversed. Outputs as ddp_bucket_assign. Host-only.
+ * DDP_ERR_ARG if walk is not a permutation. */
+ddp_status ddp_bucket_assign_order(int32_t k, const int64_t* numel, int32_t elem_size,
+                                   int64_t first_bucket_cap_bytes, int64_t bucket_cap_bytes,
+                                   const int32_t* walk, int32_t* n_buckets, int32_t* bucket_of,
+                                   int64_t* offset, int32_t* bucket_ptr, int32_t* bucket_tensors,
+                                   int64_t* bucket_numel);
+
 /* Copy each replica's k gradients into its flat bucket. [DDP] Part 2
  * "Step 2: backward", mark_variable_ready: each parameter's gradient is
  * copied into its slice of the bucket's flat tensor, optionally pre-divided.
@@ -292,6 +304,34 @@ ddp_status ddp_reducer_bucket(const ddp_reducer* handle, int32_t b, int64_t* num
 ddp_status ddp_reducer_sync(ddp_reducer* handle, float divisor, float predivide, ddp_algo algo,
                             ddp_sync_mode mode, cudaStream_t stream);
 ddp_status ddp_reducer_destroy(ddp_reducer* handle);
+
+/* Readiness-driven firing, as the Reducer's hooks do it during backward
+ * ([DDP] Part 2 "Step 2: backward": mark_variable_ready decrements the
+ * bucket's pending count; mark_bucket_ready reduces every contiguous complete
+ * bucket from next_bucket_ on, strictly in order; [DP] "Overlapping
+ * communication with the backward pass": the all-reduce runs on a separate
+ * stream while backward continues).
+ * ddp_reducer_prepare resets the pending counts and the observed order.
+ * ddp_reducer_mark_ready marks gradient `tensor` (registration index) ready:
+ *   if that completes bucket next_bucket_ (and the ones after it), each of
+ *   them is all-reduced in place (ddp_bucket_allreduce with divisor) on
+ *   comm_stream, which first waits on `ready` (if not NULL: the event after
+ *   which the gradient holds its final value; events must complete in marking
+ *   order, e.g. all recorded on one producing stream). *fired (if not NULL)
+ *   = number of buckets launched by this call. DDP_ERR_STATE if the tensor was
+ *   already marked since the last prepare.
+ * ddp_reducer_observed writes the ready order seen since the last prepare
+ *   into order (if not NULL) and returns its length (-1 for a null handle).
+ * ddp_reducer_rebuild rebuilds the buckets along `order` (a permutation of
+ *   0..k-1, first-ready first) or, if order is NULL, along the observed order
+ *   (DDP_ERR_STATE unless every tensor was marked); reallocates the flat
+ *   buckets and tables (it synchronizes the device) and resets readiness. */
+ddp_status ddp_reducer_prepare(ddp_reducer* handle);
+ddp_status ddp_reducer_mark_ready(ddp_reducer* handle, int32_t tensor, float divisor, cudaEvent_t ready,
+                                  cudaStream_t comm_stream, int32_t* fired);
+int32_t ddp_reducer_observed(const ddp_reducer* handle, int32_t* order);
+ddp_status ddp_reducer_rebuild(ddp_reducer* handle, const int32_t* order);
+
 
 /* Reduce-scatter that allocates nothing. No counterpart in the paper: it exists
  * for callers that cannot allocate device memory during a call -- for example a

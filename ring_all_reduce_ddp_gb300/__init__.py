@@ -59,6 +59,12 @@ _SIGS = {
     "ddp_reducer_bucket": [_c_vp, _c_i32, _P_i64, _P_vp],
     "ddp_reducer_sync": [_c_vp, _c_f32, _c_f32, _c_i32, _c_i32, _c_vp],
     "ddp_reducer_destroy": [_c_vp],
+    "ddp_reducer_prepare": [_c_vp],
+    "ddp_reducer_mark_ready": [_c_vp, _c_i32, _c_f32, _c_vp, _c_vp, _P_i32],
+    "ddp_reducer_observed": [_c_vp, _P_i32],
+    "ddp_reducer_rebuild": [_c_vp, _P_i32],
+    "ddp_bucket_assign_order": [_c_i32, _P_i64, _c_i32, _c_i64, _c_i64, _P_i32, _P_i32, _P_i32, _P_i64, _P_i32,
+                                _P_i32, _P_i64],
     "ddp_reduce_scatter_noalloc": [_P_vp, _P_vp, _c_i32, _c_i64, _c_i32, _c_f32, _c_i32, _c_vp],
     "ddp_broadcast": [_P_vp, _c_i32, _c_i64, _c_i32, _c_i32, _c_vp],
     "ddp_broadcast_coalesced": [_c_i32, _c_i32, _P_vp, _P_i64, _c_i32, _c_i64, _c_i32, _c_vp],
@@ -76,7 +82,7 @@ _SIGS = {
     "ddp_last_error": [],
     "ddp_status_string": [_c_i32],
 }
-_RESTYPES = {"ddp_reducer_num_buckets": _c_i32, "ddp_ring_num_steps": _c_i32, "ddp_ring_steps_done": _c_i32, "ddp_kernel_launches": _c_i64,
+_RESTYPES = {"ddp_reducer_observed": _c_i32, "ddp_reducer_num_buckets": _c_i32, "ddp_ring_num_steps": _c_i32, "ddp_ring_steps_done": _c_i32, "ddp_kernel_launches": _c_i64,
              "ddp_last_error": ctypes.c_char_p, "ddp_status_string": ctypes.c_char_p}
 
 _lib = None
@@ -177,6 +183,25 @@ def ddp_bucket_assign(numel, elem_size: int, first_bucket_cap_bytes: int, bucket
     bnumel = (ctypes.c_int64 * max(1, k))()
     _check(lib().ddp_bucket_assign(k, _i64s(numel), elem_size, first_bucket_cap_bytes, bucket_cap_bytes,
                                    order, ctypes.byref(nb), bucket_of, offset, bptr, btens, bnumel))
+    B = nb.value
+    buckets = [[btens[i] for i in range(bptr[b], bptr[b + 1])] for b in range(B)]
+    return {"buckets": buckets, "bucket_of": list(bucket_of)[:k], "offset": list(offset)[:k],
+            "bucket_numel": list(bnumel)[:B]}
+
+
+def ddp_bucket_assign_order(numel, elem_size: int, first_bucket_cap_bytes: int, bucket_cap_bytes: int,
+                            walk) -> dict:
+    """Buckets along an explicit walk (first-ready first); same result dict as ddp_bucket_assign."""
+    k = len(numel)
+    nb = ctypes.c_int32(0)
+    bucket_of = (ctypes.c_int32 * max(1, k))()
+    offset = (ctypes.c_int64 * max(1, k))()
+    bptr = (ctypes.c_int32 * (k + 1))()
+    btens = (ctypes.c_int32 * max(1, k))()
+    bnumel = (ctypes.c_int64 * max(1, k))()
+    w = (ctypes.c_int32 * max(1, k))(*[int(x) for x in walk])
+    _check(lib().ddp_bucket_assign_order(k, _i64s(numel), elem_size, first_bucket_cap_bytes, bucket_cap_bytes, w,
+                                         ctypes.byref(nb), bucket_of, offset, bptr, btens, bnumel))
     B = nb.value
     buckets = [[btens[i] for i in range(bptr[b], bptr[b + 1])] for b in range(B)]
     return {"buckets": buckets, "bucket_of": list(bucket_of)[:k], "offset": list(offset)[:k],
@@ -306,6 +331,29 @@ class DDPReducer:
              predivide: float = 1.0, stream=None):
         _check(lib().ddp_reducer_sync(self.h, float(divisor), float(predivide), int(algo), int(mode),
                                       _stream(stream)))
+
+    def prepare(self):
+        _check(lib().ddp_reducer_prepare(self.h))
+
+    def mark_ready(self, tensor: int, divisor: float, ready_event=None, comm_stream=None) -> int:
+        """Mark gradient `tensor` ready; returns how many buckets this fired.
+        ready_event: a torch.cuda.Event (or raw handle) the comm stream waits on."""
+        fired = ctypes.c_int32(0)
+        ev = 0 if ready_event is None else (ready_event if isinstance(ready_event, int)
+                                            else int(ready_event.cuda_event))
+        _check(lib().ddp_reducer_mark_ready(self.h, int(tensor), float(divisor), ev, _stream(comm_stream),
+                                            ctypes.byref(fired)))
+        return fired.value
+
+    def observed(self) -> list[int]:
+        n = lib().ddp_reducer_observed(self.h, None)
+        arr = (ctypes.c_int32 * max(1, n))()
+        lib().ddp_reducer_observed(self.h, arr)
+        return [arr[i] for i in range(n)]
+
+    def rebuild(self, order=None):
+        arr = None if order is None else (ctypes.c_int32 * len(order))(*[int(x) for x in order])
+        _check(lib().ddp_reducer_rebuild(self.h, arr))
 
     def destroy(self):
         if self.h:

@@ -506,6 +506,46 @@ ddp_status run_bucket_launches(std::vector<BucketArgs>& launches, ddp_dtype dt, 
   return DDP_OK;
 }
 
+// Write a bucket list (tensor indices per bucket, walk order) in the
+// ddp_bucket_assign output format.
+void write_assignment(const std::vector<std::vector<int32_t>>& buckets, const int64_t* numel, int32_t* n_buckets,
+                      int32_t* bucket_of, int64_t* offset, int32_t* bucket_ptr, int32_t* bucket_tensors,
+                      int64_t* bucket_numel) {
+  int32_t pos = 0;
+  bucket_ptr[0] = 0;
+  for (size_t b = 0; b < buckets.size(); ++b) {
+    int64_t off = 0;
+    for (int32_t t : buckets[b]) {
+      bucket_of[t] = static_cast<int32_t>(b);
+      offset[t] = off;
+      off += numel[t];
+      bucket_tensors[pos++] = t;
+    }
+    bucket_numel[b] = off;
+    bucket_ptr[b + 1] = pos;
+  }
+  *n_buckets = static_cast<int32_t>(buckets.size());
+}
+
+// Walk `walk` (tensor indices), closing a bucket once its bytes reach its cap.
+std::vector<std::vector<int32_t>> walk_buckets(const std::vector<int32_t>& walk, const int64_t* numel,
+                                               int32_t elem_size, int64_t first_cap, int64_t cap) {
+  std::vector<std::vector<int32_t>> buckets;
+  std::vector<int32_t> open;
+  int64_t bytes = 0;
+  for (int32_t t : walk) {
+    open.push_back(t);
+    bytes += numel[t] * elem_size;
+    if (bytes >= (buckets.empty() ? first_cap : cap)) {
+      buckets.push_back(open);
+      open.clear();
+      bytes = 0;
+    }
+  }
+  if (!open.empty()) buckets.push_back(open);
+  return buckets;
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -530,38 +570,33 @@ ddp_status ddp_bucket_assign(int32_t k, const int64_t* numel, int32_t elem_size,
   DDP_CHECK(order == DDP_ORDER_REVERSED || order == DDP_ORDER_REGISTRATION, DDP_ERR_ARG, "unknown order");
   for (int32_t t = 0; t < k; ++t) DDP_CHECK(numel[t] >= 0, DDP_ERR_ARG, "numel must be >= 0");
 
-  // Walk, closing a bucket once its bytes reach its cap.
-  std::vector<std::vector<int32_t>> buckets;
-  std::vector<int32_t> open;
-  int64_t bytes = 0;
-  for (int32_t w = 0; w < k; ++w) {
-    const int32_t t = (order == DDP_ORDER_REVERSED) ? k - 1 - w : w;
-    open.push_back(t);
-    bytes += numel[t] * elem_size;
-    const int64_t cap = buckets.empty() ? first_bucket_cap_bytes : bucket_cap_bytes;
-    if (bytes >= cap) {
-      buckets.push_back(open);
-      open.clear();
-      bytes = 0;
-    }
-  }
-  if (!open.empty()) buckets.push_back(open);
+  std::vector<int32_t> walk(k);
+  for (int32_t w = 0; w < k; ++w) walk[w] = (order == DDP_ORDER_REVERSED) ? k - 1 - w : w;
+  auto buckets = walk_buckets(walk, numel, elem_size, first_bucket_cap_bytes, bucket_cap_bytes);
   if (order == DDP_ORDER_REGISTRATION) std::reverse(buckets.begin(), buckets.end());
+  write_assignment(buckets, numel, n_buckets, bucket_of, offset, bucket_ptr, bucket_tensors, bucket_numel);
+  return DDP_OK;
+}
 
-  int32_t pos = 0;
-  bucket_ptr[0] = 0;
-  for (size_t b = 0; b < buckets.size(); ++b) {
-    int64_t off = 0;
-    for (int32_t t : buckets[b]) {
-      bucket_of[t] = static_cast<int32_t>(b);
-      offset[t] = off;
-      off += numel[t];
-      bucket_tensors[pos++] = t;
-    }
-    bucket_numel[b] = off;
-    bucket_ptr[b + 1] = pos;
+ddp_status ddp_bucket_assign_order(int32_t k, const int64_t* numel, int32_t elem_size,
+                                   int64_t first_bucket_cap_bytes, int64_t bucket_cap_bytes, const int32_t* walk,
+                                   int32_t* n_buckets, int32_t* bucket_of, int64_t* offset, int32_t* bucket_ptr,
+                                   int32_t* bucket_tensors, int64_t* bucket_numel) {
+  DDP_CHECK(k >= 0, DDP_ERR_ARG, "k must be >= 0");
+  DDP_CHECK(n_buckets && bucket_ptr, DDP_ERR_ARG, "output arrays are null");
+  DDP_CHECK(k == 0 || (numel && walk && bucket_of && offset && bucket_tensors && bucket_numel), DDP_ERR_ARG,
+            "input or output arrays are null");
+  DDP_CHECK(elem_size > 0, DDP_ERR_ARG, "elem_size must be > 0");
+  DDP_CHECK(first_bucket_cap_bytes >= 0 && bucket_cap_bytes >= 0, DDP_ERR_ARG, "caps must be >= 0");
+  std::vector<char> seen(k, 0);
+  for (int32_t w = 0; w < k; ++w) {
+    DDP_CHECK(walk[w] >= 0 && walk[w] < k && !seen[walk[w]], DDP_ERR_ARG, "walk must be a permutation of 0..k-1");
+    seen[walk[w]] = 1;
+    DDP_CHECK(numel[walk[w]] >= 0, DDP_ERR_ARG, "numel must be >= 0");
   }
-  *n_buckets = static_cast<int32_t>(buckets.size());
+  const auto buckets = walk_buckets(std::vector<int32_t>(walk, walk + k), numel, elem_size, first_bucket_cap_bytes,
+                                    bucket_cap_bytes);
+  write_assignment(buckets, numel, n_buckets, bucket_of, offset, bucket_ptr, bucket_tensors, bucket_numel);
   return DDP_OK;
 }
 
@@ -881,6 +916,7 @@ ddp_status ddp_bucket_allreduce(int32_t p, int32_t k, void* const* grads, const 
 struct ddp_reducer {
   int32_t p = 0, k = 0;
   ddp_dtype dt = DDP_FLOAT32;
+  int64_t first_cap = 0, cap = 0;
   std::vector<void*> grads;  // [p * k]
   std::vector<int64_t> numel;
   struct Bucket {
@@ -889,17 +925,35 @@ struct ddp_reducer {
     int64_t n = 0;
     std::vector<void*> flat;             // [p]
     std::vector<const void*> grads;      // [p * members], replica-major
+    std::vector<BucketArgs> launches;    // this bucket alone, in place (readiness-driven firing)
   };
   std::vector<Bucket> buckets;
+  std::vector<int32_t> bucket_of;  // per tensor
   std::vector<void*> arenas;  // one flat-bucket arena per replica
   float* ws = nullptr;        // fp32 partials for the literal bf16 schedule
   int64_t ws_elems = 0;
   void* table_mem = nullptr;  // the in-place sync's piece table, every bucket, in device memory
   BucketTable table{};
   int32_t table_tiles = 0;
+  // readiness ("PyTorch DDP Deep Dive", Part 2: pending counts, next_bucket_)
+  std::vector<int32_t> pending;
+  std::vector<char> marked;
+  std::vector<int32_t> observed;  // ready order seen since the last prepare
+  int32_t next_bucket = 0;
 };
 
 namespace {
+
+void reducer_free_device(ddp_reducer* h) {
+  for (void* a : h->arenas) cudaFree(a);
+  h->arenas.clear();
+  if (h->ws) cudaFree(h->ws);
+  h->ws = nullptr;
+  if (h->table_mem) cudaFree(h->table_mem);
+  h->table_mem = nullptr;
+  h->table = BucketTable{};
+  h->table_tiles = 0;
+}
 
 // Cut every bucket of the reducer into pieces (tensor x chunk, one summation
 // origin each), in bucket order, and upload the table to device memory once.
@@ -962,6 +1016,66 @@ ddp_status build_reducer_table(ddp_reducer* h) {
   return DDP_OK;
 }
 
+// (Re)build buckets from a walk order over the tensors: the flat-bucket
+// arenas, the bf16 workspace, each bucket's own in-place launches and the
+// whole-set piece table. Frees whatever device memory a previous build held.
+ddp_status reducer_build(ddp_reducer* h, const std::vector<int32_t>& walk, bool reverse_list) {
+  const int p = h->p, k = h->k, es = esize(h->dt);
+  auto lists = walk_buckets(walk, h->numel.data(), es, h->first_cap, h->cap);
+  if (reverse_list) std::reverse(lists.begin(), lists.end());
+  reducer_free_device(h);
+  h->buckets.clear();
+  h->bucket_of.assign(k, -1);
+  h->ws_elems = 0;
+  int64_t arena = 0;
+  std::vector<int64_t> base;
+  for (const auto& members : lists) {
+    int64_t n = 0;
+    for (int32_t t : members) n += h->numel[t];
+    base.push_back(arena);
+    arena += (n * es + 255) / 256 * 256;
+    h->ws_elems = std::max(h->ws_elems, 2 * static_cast<int64_t>(p) * chunk_size(n, p));
+  }
+  for (int32_t r = 0; r < p; ++r) {
+    void* a = nullptr;
+    const cudaError_t e = cudaMalloc(&a, std::max<int64_t>(arena, 256));
+    if (e != cudaSuccess) return fail(DDP_ERR_NOMEM, std::string("reducer buckets: ") + cudaGetErrorString(e));
+    h->arenas.push_back(a);
+  }
+  if (h->dt == DDP_BFLOAT16 && p > 1 && h->ws_elems > 0) {
+    void* w = nullptr;
+    const cudaError_t e = cudaMalloc(&w, h->ws_elems * sizeof(float));
+    if (e != cudaSuccess) return fail(DDP_ERR_NOMEM, std::string("reducer workspace: ") + cudaGetErrorString(e));
+    h->ws = static_cast<float*>(w);
+  }
+  for (size_t b = 0; b < lists.size(); ++b) {
+    ddp_reducer::Bucket B;
+    int64_t off = 0;
+    for (int32_t t : lists[b]) {
+      B.members.push_back(t);
+      B.numel.push_back(h->numel[t]);
+      B.offset.push_back(off);
+      off += h->numel[t];
+      h->bucket_of[t] = static_cast<int32_t>(b);
+    }
+    B.n = off;
+    const int32_t m = static_cast<int32_t>(B.members.size());
+    for (int32_t r = 0; r < p; ++r) {
+      B.flat.push_back(static_cast<char*>(h->arenas[r]) + base[b]);
+      for (int32_t t : B.members) B.grads.push_back(h->grads[static_cast<int64_t>(r) * k + t]);
+    }
+    DDP_TRY(plan_bucket_launches(p, m, B.grads.data(), B.numel.data(), B.offset.data(), h->dt, 1.0f, B.launches));
+    h->buckets.push_back(std::move(B));
+  }
+  DDP_TRY(build_reducer_table(h));
+  h->pending.assign(h->buckets.size(), 0);
+  for (size_t b = 0; b < h->buckets.size(); ++b) h->pending[b] = static_cast<int32_t>(h->buckets[b].members.size());
+  h->marked.assign(k, 0);
+  h->observed.clear();
+  h->next_bucket = 0;
+  return DDP_OK;
+}
+
 }  // namespace
 
 ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* const* grads,
@@ -971,14 +1085,12 @@ ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* 
   *handle = nullptr;
   DDP_TRY(check_common(p, 0, dtype));
   DDP_CHECK(k >= 1 && numel && grads, DDP_ERR_ARG, "need k >= 1 tensors, numel and grads");
+  DDP_CHECK(first_bucket_cap_bytes >= 0 && bucket_cap_bytes >= 0, DDP_ERR_ARG, "caps must be >= 0");
+  DDP_CHECK(order == DDP_ORDER_REVERSED || order == DDP_ORDER_REGISTRATION, DDP_ERR_ARG, "unknown order");
   const int es = esize(dtype);
-  std::vector<int32_t> bucket_of(k), bptr(k + 1), btens(k);
-  std::vector<int64_t> offset(k), bnumel(k);
-  int32_t nb = 0;
-  DDP_TRY(ddp_bucket_assign(k, numel, es, first_bucket_cap_bytes, bucket_cap_bytes, order, &nb, bucket_of.data(),
-                            offset.data(), bptr.data(), btens.data(), bnumel.data()));
   {
     std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
+    for (int32_t t = 0; t < k; ++t) DDP_CHECK(numel[t] >= 0, DDP_ERR_ARG, "numel must be >= 0");
     for (int32_t r = 0; r < p; ++r)
       for (int32_t t = 0; t < k; ++t) {
         if (numel[t] == 0) continue;
@@ -990,53 +1102,17 @@ ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* 
   }
   ddp_reducer* h = new ddp_reducer();
   h->p = p; h->k = k; h->dt = dtype;
+  h->first_cap = first_bucket_cap_bytes;
+  h->cap = bucket_cap_bytes;
   h->grads.assign(grads, grads + static_cast<int64_t>(p) * k);
   h->numel.assign(numel, numel + k);
-  int64_t arena = 0;
-  std::vector<int64_t> base(nb);
-  for (int32_t b = 0; b < nb; ++b) {
-    base[b] = arena;
-    arena += (bnumel[b] * es + 255) / 256 * 256;
-    h->ws_elems = std::max(h->ws_elems, 2 * static_cast<int64_t>(p) * chunk_size(bnumel[b], p));
-  }
-  auto fail_free = [&](ddp_status st, const std::string& msg) {
-    for (void* a : h->arenas) cudaFree(a);
-    if (h->ws) cudaFree(h->ws);
-    if (h->table_mem) cudaFree(h->table_mem);
+  std::vector<int32_t> walk(k);
+  for (int32_t w = 0; w < k; ++w) walk[w] = (order == DDP_ORDER_REVERSED) ? k - 1 - w : w;
+  const ddp_status st = reducer_build(h, walk, order == DDP_ORDER_REGISTRATION);
+  if (st != DDP_OK) {
+    reducer_free_device(h);
     delete h;
-    return fail(st, msg);
-  };
-  for (int32_t r = 0; r < p; ++r) {
-    void* a = nullptr;
-    const cudaError_t e = cudaMalloc(&a, std::max<int64_t>(arena, 256));
-    if (e != cudaSuccess) return fail_free(DDP_ERR_NOMEM, std::string("reducer buckets: ") + cudaGetErrorString(e));
-    h->arenas.push_back(a);
-  }
-  if (dtype == DDP_BFLOAT16 && p > 1 && h->ws_elems > 0) {
-    void* w = nullptr;
-    const cudaError_t e = cudaMalloc(&w, h->ws_elems * sizeof(float));
-    if (e != cudaSuccess) return fail_free(DDP_ERR_NOMEM, std::string("reducer workspace: ") + cudaGetErrorString(e));
-    h->ws = static_cast<float*>(w);
-  }
-  for (int32_t b = 0; b < nb; ++b) {
-    ddp_reducer::Bucket B;
-    B.n = bnumel[b];
-    for (int32_t i = bptr[b]; i < bptr[b + 1]; ++i) {
-      const int32_t t = btens[i];
-      B.members.push_back(t);
-      B.numel.push_back(numel[t]);
-      B.offset.push_back(offset[t]);
-    }
-    const int32_t m = static_cast<int32_t>(B.members.size());
-    for (int32_t r = 0; r < p; ++r) {
-      B.flat.push_back(static_cast<char*>(h->arenas[r]) + base[b]);
-      for (int32_t t : B.members) B.grads.push_back(grads[static_cast<int64_t>(r) * k + t]);
-    }
-    h->buckets.push_back(std::move(B));
-  }
-  {
-    const ddp_status st = build_reducer_table(h);
-    if (st != DDP_OK) return fail_free(st, t_error);
+    return st;
   }
   *handle = h;
   return DDP_OK;
@@ -1103,24 +1179,73 @@ ddp_status ddp_reducer_sync(ddp_reducer* h, float divisor, float predivide, ddp_
 
 ddp_status ddp_reducer_destroy(ddp_reducer* h) {
   if (!h) return DDP_OK;
-  cudaError_t e = cudaSuccess;
-  for (void* a : h->arenas) {
-    const cudaError_t e2 = cudaFree(a);
-    if (e == cudaSuccess) e = e2;
-  }
-  if (h->ws) {
-    const cudaError_t e2 = cudaFree(h->ws);
-    if (e == cudaSuccess) e = e2;
-  }
-  if (h->table_mem) {
-    const cudaError_t e2 = cudaFree(h->table_mem);
-    if (e == cudaSuccess) e = e2;
-  }
+  reducer_free_device(h);
   delete h;
+  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "reducer release");
   return DDP_OK;
 }
 
+ddp_status ddp_reducer_prepare(ddp_reducer* h) {
+  DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
+  for (size_t b = 0; b < h->buckets.size(); ++b) h->pending[b] = static_cast<int32_t>(h->buckets[b].members.size());
+  std::fill(h->marked.begin(), h->marked.end(), 0);
+  h->observed.clear();
+  h->next_bucket = 0;
+  return DDP_OK;
+}
+
+ddp_status ddp_reducer_mark_ready(ddp_reducer* h, int32_t tensor, float divisor, cudaEvent_t ready,
+                                  cudaStream_t comm_stream, int32_t* fired) {
+  DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
+  DDP_CHECK(tensor >= 0 && tensor < h->k, DDP_ERR_ARG, "tensor index out of range");
+  DDP_TRY(check_divisor(divisor));
+  DDP_CHECK(!h->marked[tensor], DDP_ERR_STATE,
+            "tensor " + std::to_string(tensor) + " was already marked ready since the last ddp_reducer_prepare");
+  h->marked[tensor] = 1;
+  h->observed.push_back(tensor);
+  h->pending[h->bucket_of[tensor]] -= 1;
+  int32_t n = 0;
+  bool waited = false;
+  const int32_t nb = static_cast<int32_t>(h->buckets.size());
+  while (h->next_bucket < nb && h->pending[h->next_bucket] == 0) {  // mark_bucket_ready: strictly in order
+    if (ready && !waited) {
+      DDP_CUDA(cudaStreamWaitEvent(comm_stream, ready, 0), "wait on the gradient's ready event");
+      waited = true;
+    }
+    DDP_TRY(run_bucket_launches(h->buckets[h->next_bucket].launches, h->dt, divisor, comm_stream));
+    ++h->next_bucket;
+    ++n;
+  }
+  if (fired) *fired = n;
+  return DDP_OK;
+}
+
+int32_t ddp_reducer_observed(const ddp_reducer* h, int32_t* order) {
+  if (!h) return -1;
+  if (order)
+    for (size_t i = 0; i < h->observed.size(); ++i) order[i] = h->observed[i];
+  return static_cast<int32_t>(h->observed.size());
+}
+
+ddp_status ddp_reducer_rebuild(ddp_reducer* h, const int32_t* order) {
+  DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
+  std::vector<int32_t> walk;
+  if (order) {
+    walk.assign(order, order + h->k);
+  } else {
+    DDP_CHECK(static_cast<int32_t>(h->observed.size()) == h->k, DDP_ERR_STATE,
+              "rebuild from the observed order needs every tensor marked ready since the last prepare");
+    walk = h->observed;
+  }
+  std::vector<char> seen(h->k, 0);
+  for (int32_t t : walk) {
+    DDP_CHECK(t >= 0 && t < h->k && !seen[t], DDP_ERR_ARG, "order must be a permutation of 0..k-1");
+    seen[t] = 1;
+  }
+  DDP_CUDA(cudaDeviceSynchronize(), "synchronize before rebuilding buckets");
+  return reducer_build(h, walk, false);
+}
 
 ddp_status ddp_allreduce_persistent(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
                                     int64_t timeout_ns, int32_t fault_rank, int32_t fault_step, int32_t* status,

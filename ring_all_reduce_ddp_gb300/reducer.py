@@ -16,7 +16,7 @@ from __future__ import annotations
 import ctypes
 
 from . import (DDP_ALGO_FUSED, DDP_ORDER_REVERSED, DDP_SYNC_IN_PLACE, DDPReducer, _ptrs, _i64s,
-               ddp_broadcast_coalesced, ddp_bucket_assign)
+               ddp_broadcast_coalesced, ddp_bucket_assign, ddp_bucket_assign_order)
 
 MiB = 1 << 20
 
@@ -32,6 +32,7 @@ class Reducer(DDPReducer):
         self.esize = grads[0][0].element_size()
         self.numel = [g.numel() for g in grads[0]]
         self._caps = (first_bucket_cap_bytes, bucket_cap_bytes, order)
+        self._walk = None
         plan = ddp_bucket_assign(self.numel, self.esize, *self._caps)
         self.plan = plan
         self.buckets = plan["buckets"]
@@ -41,7 +42,24 @@ class Reducer(DDPReducer):
 
     def assign(self) -> bool:
         """Recompute the bucket assignment (host only); True if it is unchanged."""
-        return ddp_bucket_assign(self.numel, self.esize, *self._caps)["buckets"] == self.buckets
+        if self._walk is not None:
+            got = ddp_bucket_assign_order(self.numel, self.esize, self._caps[0], self._caps[1], self._walk)
+        else:
+            got = ddp_bucket_assign(self.numel, self.esize, *self._caps)
+        return got["buckets"] == self.buckets
+
+    def rebuild(self, order=None):
+        """Rebuild the buckets along `order`, or along the ready order observed
+        since the last prepare(), and refresh the host-side plan."""
+        walk = list(order) if order is not None else self.observed()
+        super().rebuild(order)
+        self._walk = walk
+        plan = ddp_bucket_assign_order(self.numel, self.esize, self._caps[0], self._caps[1], walk)
+        self.plan = plan
+        self.buckets = plan["buckets"]
+        self.bucket_numel = plan["bucket_numel"]
+        self.offset = plan["offset"]
+        assert self.num_buckets() == len(self.buckets)
 
     def sync_gradients(self, divisor: float, algo: int = DDP_ALGO_FUSED, mode: int = DDP_SYNC_IN_PLACE,
                        predivide: float = 1.0, stream=None):

@@ -91,3 +91,18 @@ def test_argument_errors_are_reported_before_any_launch(L):
     assert lib.ddp_broadcast(arr, 2, 16, 5, 0, None) == L.DDP_ERR_ARG                # root out of range
     # zero-size work is a no-op that touches no device
     assert lib.ddp_allreduce(arr, 2, 0, 0, 1.0, 0, None) == L.DDP_OK
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_bucket_assign_order_matches_oracle_rebuild(L, seed):
+    import numpy as np
+    from oracle import reducer_sim as rs
+    rng = np.random.default_rng(seed)
+    k = int(rng.integers(1, 40))
+    numel = [int(x) for x in rng.integers(0, 5000, size=k)]
+    walk = [int(x) for x in rng.permutation(k)]
+    first, cap = int(rng.integers(0, 20000)), int(rng.integers(1, 60000))
+    got = L.ddp_bucket_assign_order(numel, 4, first, cap, walk)
+    assert got["buckets"] == rs.rebuild(numel, 4, first, cap, walk)
+    with pytest.raises(L.DDPError):
+        L.ddp_bucket_assign_order(numel, 4, first, cap, walk[:-1] + [walk[0]] if k > 1 else [5])

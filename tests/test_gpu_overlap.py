@@ -1,0 +1,99 @@
+"""Readiness-driven bucket all-reduces on a communication stream (GPU).
+
+Gradients are marked ready one by one, each with an event recorded on the
+producing stream; the Reducer must fire buckets strictly in order exactly
+when the oracle's replay of mark_variable_ready / mark_bucket_ready says,
+and the result must be the bits of a whole-set sync. A rebuild from the
+observed ready order must give the oracle's rebuilt buckets and still reduce
+to the oracle's values."""
+import numpy as np
+import pytest
+
+import ring_all_reduce_ddp_gb300 as D
+from oracle import buckets as ob
+from oracle import reducer_sim as rs
+from oracle import ring as orc
+from ring_all_reduce_ddp_gb300.reducer import Reducer
+from synth import workloads as W
+from tests.helpers import assert_bit_equal, to_host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _fire_positions(red, order, divisor, comm, compute):
+    seq = []
+    fired_total = 0
+    for pos, t in enumerate(order):
+        ev = torch.cuda.Event()
+        ev.record(compute)
+        n = red.mark_ready(t, divisor, ev, comm)
+        seq += [(pos, fired_total + i) for i in range(n)]
+        fired_total += n
+    return seq
+
+
+@pytest.mark.parametrize("shuffle", [False, True])
+def test_mark_ready_fires_like_the_reducer_and_reduces_like_a_sync(shuffle):
+    cfg = W.CONFIGS["resnet50"]
+    grads, _ = W.make_grads(cfg)
+    ref_grads, _ = W.make_grads(cfg)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    ref = Reducer(ref_grads, cfg["first_cap"], cfg["cap"])
+    Dv = W.divisor(cfg)
+    ref.sync_gradients(Dv, D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE)
+    k = len(grads[0])
+    order = list(range(k))[::-1]
+    if shuffle:
+        order = [int(x) for x in np.random.default_rng(3).permutation(k)]
+    comm = torch.cuda.Stream()
+    compute = torch.cuda.current_stream()
+    red.prepare()
+    seq = _fire_positions(red, order, Dv, comm, compute)
+    torch.cuda.synchronize()
+    assert seq == rs.fire_sequence(red.buckets, order)
+    assert red.observed() == order
+    for r in range(cfg["p"]):
+        for t in range(k):
+            assert torch.equal(grads[r][t].view(torch.int32), ref_grads[r][t].view(torch.int32)), (r, t)
+    with pytest.raises(D.DDPError) as e:
+        red.mark_ready(order[0], Dv, None, comm)
+    assert e.value.status == D.DDP_ERR_STATE
+    assert D.ddp_device_error() == 0
+
+
+def test_rebuild_from_the_observed_order():
+    cfg = W.CONFIGS["tiny"]
+    p = cfg["p"]
+    grads, _ = W.make_grads(cfg)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    numel = W.numels(cfg)
+    observed = [9, 0, 8, 1, 7, 2, 6, 3, 5, 4]
+    red.prepare()
+    comm = torch.cuda.Stream()
+    for t in observed:  # readiness only: the in-place reduction of this pass is checked above
+        red.mark_ready(t, 1.0, None, comm)
+    torch.cuda.synchronize()
+    red.rebuild()  # along the observed order
+    want_buckets = rs.rebuild(numel, 4, cfg["first_cap"], cfg["cap"], observed)
+    assert red.buckets == want_buckets
+    # fresh gradients, one sync on the rebuilt buckets, every element against the oracle
+    fresh, _ = W.make_grads(cfg)
+    for r in range(p):
+        for t in range(len(numel)):
+            grads[r][t].copy_(fresh[r][t])
+    red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE)
+    torch.cuda.synchronize()
+    starts = W.tensor_starts(cfg)
+    _, offset, bnumel = ob.bucket_layout(numel, want_buckets)
+    for b, members in enumerate(want_buckets):
+        ins = []
+        for r in range(p):
+            hv = {t: W.host_values(cfg, r, np.arange(starts[t], starts[t] + numel[t])) for t in members}
+            ins.append(ob.flatten([hv.get(t, np.zeros(0, np.float32)) for t in range(len(numel))], members,
+                                  offset, bnumel[b]))
+        want, _ = orc.allreduce(ins, bnumel[b], W.divisor(cfg))
+        for r in range(p):
+            back = ob.unflatten(want[r], members, offset, numel)
+            for t in members:
+                assert_bit_equal(to_host(grads[r][t]), back[t], f"tensor {t} replica {r}")
