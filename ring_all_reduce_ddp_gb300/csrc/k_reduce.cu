@@ -403,21 +403,46 @@ __global__ void __launch_bounds__(kThreads) k_rs_step_inplace_f32(const __grid_c
   const float* xs = reinterpret_cast<const float*>(a.x[r]) + lo;
   float* xd = reinterpret_cast<float*>(a.x[d]) + lo;
   const int64_t len = hi - lo;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads * kU; base < len;
-       base += static_cast<int64_t>(gridDim.x) * kThreads * kU) {
-    float loc[kU], rcv[kU];
+  auto one = [&](int64_t e) {
+    float y = __fadd_rn(xd[e], xs[e]);
+    if (a.last) y = __fdiv_rn(y, a.divisor);
+    xd[e] = y;
+  };
+  // 16-byte vectors where both replicas sit at the same address mod 16
+  int64_t head = len;
+  const uintptr_t ad = reinterpret_cast<uintptr_t>(xd), as = reinterpret_cast<uintptr_t>(xs);
+  if (((ad ^ as) & 15u) == 0 && (ad & 3u) == 0) head = min(static_cast<int64_t>(((16u - (ad & 15u)) & 15u) / 4), len);
+  const int64_t nvec = (len - head) / 4;
+  const int64_t tail0 = head + nvec * 4;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t gstride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t e = gtid; e < head; e += gstride) one(e);
+  for (int64_t e = tail0 + gtid; e < len; e += gstride) one(e);
+  const float4* s4 = reinterpret_cast<const float4*>(xs + head);
+  float4* d4 = reinterpret_cast<float4*>(xd + head);
+  for (int64_t v0 = gtid; v0 < nvec; v0 += gstride * kU) {
+    float4 loc[kU], rcv[kU];
 #pragma unroll
     for (int q = 0; q < kU; ++q) {
-      const int64_t e = base + q * kThreads + threadIdx.x;
-      if (e < len) { loc[q] = xd[e]; rcv[q] = xs[e]; }
+      const int64_t v = v0 + q * gstride;
+      if (v < nvec) { loc[q] = d4[v]; rcv[q] = s4[v]; }
     }
 #pragma unroll
     for (int q = 0; q < kU; ++q) {
-      const int64_t e = base + q * kThreads + threadIdx.x;
-      if (e < len) {
-        float y = __fadd_rn(loc[q], rcv[q]);
-        if (a.last) y = __fdiv_rn(y, a.divisor);
-        xd[e] = y;
+      const int64_t v = v0 + q * gstride;
+      if (v < nvec) {
+        float4 y;
+        y.x = __fadd_rn(loc[q].x, rcv[q].x);
+        y.y = __fadd_rn(loc[q].y, rcv[q].y);
+        y.z = __fadd_rn(loc[q].z, rcv[q].z);
+        y.w = __fadd_rn(loc[q].w, rcv[q].w);
+        if (a.last) {
+          y.x = __fdiv_rn(y.x, a.divisor);
+          y.y = __fdiv_rn(y.y, a.divisor);
+          y.z = __fdiv_rn(y.z, a.divisor);
+          y.w = __fdiv_rn(y.w, a.divisor);
+        }
+        d4[v] = y;
       }
     }
   }
@@ -540,7 +565,7 @@ __global__ void __launch_bounds__(kThreads) k_ring_persistent_f32(const __grid_c
     const int64_t x0 = min(hi, lo + static_cast<int64_t>(b) * span);
     const int64_t x1 = min(hi, x0 + span);
     const bool last_rs = (t == p - 2);
-    for (int64_t i = x0 + threadIdx.x; i < x1; i += blockDim.x) {
+    auto one = [&](int64_t i) {
       const float recv = __ldcg(theirs + i);
       if (rs) {
         float y = __fadd_rn(mine[i], recv);
@@ -548,6 +573,36 @@ __global__ void __launch_bounds__(kThreads) k_ring_persistent_f32(const __grid_c
         mine[i] = y;
       } else {
         mine[i] = recv;
+      }
+    };
+    // 16-byte vectors where both replicas sit at the same address mod 16
+    int64_t head = x1 - x0;
+    const uintptr_t am = reinterpret_cast<uintptr_t>(mine + x0), at = reinterpret_cast<uintptr_t>(theirs + x0);
+    if (((am ^ at) & 15u) == 0 && (am & 3u) == 0)
+      head = min(static_cast<int64_t>(((16u - (am & 15u)) & 15u) / 4), x1 - x0);
+    const int64_t nvec = (x1 - x0 - head) / 4;
+    const int64_t tail0 = x0 + head + nvec * 4;
+    for (int64_t e = threadIdx.x; e < head; e += blockDim.x) one(x0 + e);
+    for (int64_t i = tail0 + threadIdx.x; i < x1; i += blockDim.x) one(i);
+    float4* m4 = reinterpret_cast<float4*>(mine + x0 + head);
+    const float4* t4 = reinterpret_cast<const float4*>(theirs + x0 + head);
+    for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x) {
+      const float4 rcv = __ldcg(t4 + v);
+      if (rs) {
+        float4 y = m4[v];
+        y.x = __fadd_rn(y.x, rcv.x);
+        y.y = __fadd_rn(y.y, rcv.y);
+        y.z = __fadd_rn(y.z, rcv.z);
+        y.w = __fadd_rn(y.w, rcv.w);
+        if (last_rs) {
+          y.x = __fdiv_rn(y.x, a.divisor);
+          y.y = __fdiv_rn(y.y, a.divisor);
+          y.z = __fdiv_rn(y.z, a.divisor);
+          y.w = __fdiv_rn(y.w, a.divisor);
+        }
+        m4[v] = y;
+      } else {
+        m4[v] = rcv;
       }
     }
     __syncthreads();
@@ -689,7 +744,7 @@ cudaError_t launch_fused_reduce(const FusedArgs& a, ddp_dtype dt, bool staged, c
 }
 
 cudaError_t launch_rs_step_inplace_f32(const RingStepArgs& a, cudaStream_t s) {
-  const dim3 grid(blocks_per_chunk(a.cs, kThreads * kU, a.p), a.p);
+  const dim3 grid(blocks_per_chunk(a.cs / 4 + 1, kThreads * kU, a.p), a.p);
   k_rs_step_inplace_f32<<<grid, kThreads, 0, s>>>(a);
   count_launch();
   return cudaGetLastError();
