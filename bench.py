@@ -57,7 +57,7 @@ NCU_TRAFFIC = {"kernel_sha256": "c9dda4587c6463d534357f1b02194bef9056d140cfcd7eb
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="resnet50", choices=sorted(WORKLOAD_TEXT))
@@ -113,7 +113,7 @@ class Ranks:
 # --------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
-    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
@@ -131,7 +131,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
-                 "-i", ident, "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-i", ident, "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
         except FileNotFoundError:
@@ -141,7 +141,9 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self) -> dict | None:
+    def stop(self, window=None) -> dict | None:
+        """Median SM clock and active throttle reasons over the samples taken
+        inside window = (start, end) host wall-clock seconds (all samples if None)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -150,24 +152,35 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self._t.join(timeout=2)
-        sm, mx, reasons = [], [], set()
+        rows = self._parse(window)
+        in_window = window is not None and bool(rows)
+        if not rows:  # clock skew between nvidia-smi and the host: report every sample
+            rows = self._parse(None)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [r[0] for r in rows]
+        reasons = sorted(set().union(*[r[2] for r in rows]))
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows), "in_timed_window": in_window}
+
+    def _parse(self, window):
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) != len(self.FIELDS):
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                when = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, clk_max = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[4:]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            if window is not None and not (window[0] - 0.05 <= when <= window[1] + 0.05):
+                continue
+            active = {nm for nm, v in zip(names, parts[5:]) if v.lower().startswith("active")}
+            rows.append((clk, clk_max, active))
+        return rows
 
 
 # --------------------------------------------------------------- helpers
@@ -300,14 +313,16 @@ def run_ours(args, ranks: Ranks):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     ranks.barrier()
+    w0 = time.time()
     e0.record(stream)
     for _ in range(args.steps):
         step(sync_events)
     e1.record(stream)
     torch.cuda.synchronize()
+    w1 = time.time()
     ranks.barrier()
     launches = D.ddp_kernel_launches() - launches0
-    clocks = sampler.stop()
+    clocks = sampler.stop((w0, w1))
     ms = e0.elapsed_time(e1)
     ms_max = ranks.max(ms)
     ms_per_step = ms_max / args.steps
@@ -371,9 +386,10 @@ def run_ours(args, ranks: Ranks):
     torch.cuda.synchronize()
     ranks.barrier()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k_e2e = min(args.steps, 300)
     f0.record(h2d_s)
     stream.wait_stream(h2d_s)
-    for i in range(args.steps):
+    for i in range(k_e2e):
         e2e_step(i)
     stream.wait_stream(d2h_s)
     f1.record(stream)
@@ -381,8 +397,9 @@ def run_ours(args, ranks: Ranks):
     ranks.barrier()
     e2e_ms = ranks.max(f0.elapsed_time(f1))
     io = sum(a.numel() * a.element_size() for a in arenas)
-    e2e = {"value": round(step_bytes * args.steps * ranks.world / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
-           "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "ms_per_step": round(e2e_ms / args.steps, 4),
+    e2e = {"value": round(step_bytes * k_e2e * ranks.world / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+           "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "ms_per_step": round(e2e_ms / k_e2e, 4),
+           "steps": k_e2e,
            "pipeline": "step i's copy-out overlaps step i+1's copy-in (two device copies, three streams)"}
     del red_b, grads_b, arenas_b
 
