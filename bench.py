@@ -403,6 +403,29 @@ def run_ours(args, ranks: Ranks):
            "pipeline": "step i's copy-out overlaps step i+1's copy-in (two device copies, three streams)"}
     del red_b, grads_b, arenas_b
 
+    # the same step body (buffer broadcast + sync) captured once as a CUDA graph
+    # and replayed: what host launch overhead costs the eager step
+    graph = None
+    if mode == D.DDP_SYNC_IN_PLACE and ranks.world == 1:
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            if bsync:
+                bsync(bc_algo, None)
+            red.sync_gradients(divisor, algo, mode, 1.0, None)
+        for _ in range(3):
+            cg.replay()
+        torch.cuda.synchronize()
+        k_g = min(args.steps, 2000)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(k_g):
+            cg.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph = {"ms_per_step": round(g0.elapsed_time(g1) / k_g, 5), "steps": k_g,
+                 "note": "buffer broadcast + in-place sync replayed from one CUDA graph (bucket assignment stays on the host)"}
+        del cg
+
     # the three-kernel form of the same step, for comparison (not the headline)
     other = None
     if mode == D.DDP_SYNC_IN_PLACE:
@@ -448,6 +471,7 @@ def run_ours(args, ranks: Ranks):
         "busbw_gbs": round(sum(n * esz for n in red.bucket_numel) / (statistics.mean(sync_ms) / 1e3) / 1e9
                            * 2 * (p - 1) / p, 1),
         "flatten_form": other,
+        "cuda_graph": graph,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
     if ranks.rank == 0:

@@ -944,15 +944,23 @@ struct ddp_reducer {
 
 namespace {
 
-void reducer_free_device(ddp_reducer* h) {
-  for (void* a : h->arenas) cudaFree(a);
+// Free the reducer's device memory; returns the first cudaFree error.
+cudaError_t reducer_free_device(ddp_reducer* h) {
+  cudaError_t first = cudaSuccess;
+  auto release = [&](void* ptr) {
+    if (!ptr) return;
+    const cudaError_t e = cudaFree(ptr);
+    if (first == cudaSuccess) first = e;
+  };
+  for (void* a : h->arenas) release(a);
   h->arenas.clear();
-  if (h->ws) cudaFree(h->ws);
+  release(h->ws);
   h->ws = nullptr;
-  if (h->table_mem) cudaFree(h->table_mem);
+  release(h->table_mem);
   h->table_mem = nullptr;
   h->table = BucketTable{};
   h->table_tiles = 0;
+  return first;
 }
 
 // Cut every bucket of the reducer into pieces (tensor x chunk, one summation
@@ -1023,7 +1031,7 @@ ddp_status reducer_build(ddp_reducer* h, const std::vector<int32_t>& walk, bool 
   const int p = h->p, k = h->k, es = esize(h->dt);
   auto lists = walk_buckets(walk, h->numel.data(), es, h->first_cap, h->cap);
   if (reverse_list) std::reverse(lists.begin(), lists.end());
-  reducer_free_device(h);
+  DDP_CUDA(reducer_free_device(h), "reducer rebuild: release");
   h->buckets.clear();
   h->bucket_of.assign(k, -1);
   h->ws_elems = 0;
@@ -1179,9 +1187,8 @@ ddp_status ddp_reducer_sync(ddp_reducer* h, float divisor, float predivide, ddp_
 
 ddp_status ddp_reducer_destroy(ddp_reducer* h) {
   if (!h) return DDP_OK;
-  reducer_free_device(h);
+  const cudaError_t e = reducer_free_device(h);
   delete h;
-  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "reducer release");
   return DDP_OK;
 }

@@ -12,6 +12,8 @@
 // same bits as the ring on the flat bucket. Work is cut into pieces (a tensor
 // intersected with a chunk: one origin each) and pieces into tiles of
 // kBucketTileBytes per replica; a persistent grid strides over the tiles.
+#include <atomic>
+
 #include "launch.h"
 
 namespace ddp {
@@ -138,20 +140,22 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce_table(const Bucke
 // tile. The occupancy of each kernel instantiation is looked up once per device.
 template <typename T, int P, bool kTable>
 int persistent_grid(int32_t tiles) {
-  static int per_sm[64] = {0};
+  static std::atomic<int> per_sm[64];  // zero-initialised (static storage)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (per_sm[dev] == 0) {
+  int cached = per_sm[dev].load(std::memory_order_relaxed);
+  if (cached == 0) {
     int blocks = 0;
     cudaError_t e;
     if constexpr (kTable)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_bucket_allreduce_table<T, P>, kThreads, 0);
     else
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_bucket_allreduce<T, P>, kThreads, 0);
-    per_sm[dev] = (e == cudaSuccess && blocks > 0) ? blocks : 1;
+    cached = (e == cudaSuccess && blocks > 0) ? blocks : 1;
+    per_sm[dev].store(cached, std::memory_order_relaxed);
   }
-  const int64_t g = static_cast<int64_t>(per_sm[dev]) * sm_count();
+  const int64_t g = static_cast<int64_t>(cached) * sm_count();
   return static_cast<int>(g < tiles ? g : tiles);
 }
 

@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(kThreads) k_ring_persistent_f32(const __grid_c
 // ------------------------------------------------------------- launchers
 namespace {
 std::atomic<int64_t> g_launches{0};
-int g_sm_count[64] = {0};
+std::atomic<int> g_sm_count[64];  // zero-initialised (static storage)
 
 int blocks_per_chunk(int64_t work_items, int per_block, int chunks) {
   const int64_t target = static_cast<int64_t>(sm_count()) * (2048 / kThreads);
@@ -651,12 +651,14 @@ int sm_count() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (g_sm_count[dev] == 0) {
+  int c = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
     int v = 0;
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    g_sm_count[dev] = v > 0 ? v : 1;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    g_sm_count[dev].store(v, std::memory_order_relaxed);
+    c = v;
   }
-  return g_sm_count[dev];
+  return c;
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -715,14 +717,14 @@ bool plan_staged(const FusedArgs& f, StagedArgs& a) {
 template <typename T>
 cudaError_t fused_staged(const StagedArgs& a, cudaStream_t s) {
   const size_t smem = 128 + static_cast<size_t>(a.stages) * a.p * a.tile_elems * sizeof(T);
-  static bool configured[64] = {false};
+  static std::atomic<bool> configured[64];  // per device; setting the attribute twice is harmless
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     const cudaError_t e = cudaFuncSetAttribute(k_fused_reduce_staged<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                kStagedSmemBudget + 1024);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   int grid = sm_count();
   if (a.tile0[a.p] < grid) grid = a.tile0[a.p] > a.p ? a.tile0[a.p] : a.p;

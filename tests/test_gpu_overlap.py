@@ -97,3 +97,51 @@ def test_rebuild_from_the_observed_order():
             back = ob.unflatten(want[r], members, offset, numel)
             for t in members:
                 assert_bit_equal(to_host(grads[r][t]), back[t], f"tensor {t} replica {r}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "resnet50"])
+def test_step_captured_in_a_cuda_graph_replays_bit_exactly(name):
+    """The per-forward buffer broadcast and the in-place sync make no
+    allocation and no synchronisation, so one step captures into a CUDA graph;
+    replaying it gives the bits of the eager step."""
+    from ring_all_reduce_ddp_gb300.reducer import BufferSync
+    cfg = W.CONFIGS[name]
+    p = cfg["p"]
+    Dv = W.divisor(cfg)
+    eager, _ = W.make_grads(cfg)
+    graphed, _ = W.make_grads(cfg)
+    red_e = Reducer(eager, cfg["first_cap"], cfg["cap"])
+    red_g = Reducer(graphed, cfg["first_cap"], cfg["cap"])
+    bufs_e = W.buffer_set(cfg) if cfg.get("buffers") else None
+    bufs_g = W.buffer_set(cfg) if cfg.get("buffers") else None
+    bs_e = BufferSync(bufs_e) if bufs_e else None
+    bs_g = BufferSync(bufs_g) if bufs_g else None
+    # warm up (first-use lookups happen outside the capture), then restore the inputs
+    red_g.sync_gradients(Dv)
+    fresh, _ = W.make_grads(cfg)
+    torch.cuda.synchronize()
+    for r in range(p):
+        for t in range(len(fresh[r])):
+            graphed[r][t].copy_(fresh[r][t])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        if bs_g:
+            bs_g()
+        red_g.sync_gradients(Dv)
+    for r in range(p):  # capture does not run the work: inputs are still the fresh ones
+        for t in range(len(fresh[r])):
+            assert torch.equal(graphed[r][t], fresh[r][t])
+    g.replay()
+    if bs_e:
+        bs_e()
+    red_e.sync_gradients(Dv)
+    torch.cuda.synchronize()
+    for r in range(p):
+        for t in range(len(eager[r])):
+            assert torch.equal(graphed[r][t].view(torch.int16 if graphed[r][t].dtype == torch.bfloat16
+                                                  else torch.int32),
+                               eager[r][t].view(torch.int16 if eager[r][t].dtype == torch.bfloat16 else torch.int32))
+    if bufs_e:
+        for r in range(p):
+            for j in range(len(bufs_e[r])):
+                assert torch.equal(bufs_g[r][j], bufs_e[r][j])
