@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -50,8 +51,8 @@ WORKLOAD_TEXT = {
 # DRAM traffic of the dominant kernel (the in-place bucket all-reduce) from an
 # ncu capture, as bytes per algorithmic byte; valid only while the kernel
 # source it was taken on is unchanged (checked by hash).
-NCU_TRAFFIC = {"kernel_sha256": "c9dda4587c6463d534357f1b02194bef9056d140cfcd7ebdf5f3e762bbd25a5a",
-               "dram_bytes_per_algorithmic_byte": 1575.55 / 1636.13}  # ncu: read 817.9 + write 757.7 MB per launch
+NCU_TRAFFIC = {"kernel_sha256": "306a0014be0eda56d12afdb67c07755a40ba63cb21fb9f9c0a2727cd6f2ee3d7",
+               "dram_bytes_per_algorithmic_byte": (817.896704 + 757.408) / 1635.650048}  # ncu: read + write MB per launch
 
 
 def parse_args():
@@ -540,9 +541,19 @@ def run_sweep(args, ranks: Ranks):
     """Message-size / rank-count sweep: one fp32 buffer of M = 1 KiB * 4^k bytes
     on each of p replicas (p * M <= 64 GiB), values uniform on [-1, 1);
     all-reduce, reduce-scatter (both ownerships), all-gather and broadcast in
-    the fused and the literal form. One JSON line per point: median of the
-    per-launch CUDA-event times, L2 flushed (a 512 MiB write) before each
-    launch whose working set is under 2x L2."""
+    the fused and the literal form, and the tree-shaped all-reduces. One JSON
+    line per point.
+
+    Timing. Each point runs batches of `reps` launches back to back, each
+    launch on its own copy of the inputs when the working set is under 2x L2
+    (copies rotate through at most 4 GiB), so no launch finds its inputs in L2
+    and every write-back a launch leaves is paid by a later launch of the same
+    batch. Before each batch L2 is flushed: a 512 MiB write, then a 512 MiB
+    read of another buffer, so the batch starts with clean lines that belong
+    to neither. `us` = median over batches of (batch time / reps), the batch
+    captured once in a CUDA graph and replayed (host launch cost excluded);
+    `us_eager` = the same batch launched from the host. The persistent ring is
+    timed eagerly only."""
     import torch
 
     import ring_all_reduce_ddp_gb300 as D
@@ -554,69 +565,118 @@ def run_sweep(args, ranks: Ranks):
     torch.cuda.set_device(0)
     peak, peak_kind = peak_hbm()
     ps = [int(x) for x in os.environ.get("SWEEP_P", "2,4,8,16,64").split(",")]
+    min_k = int(os.environ.get("SWEEP_MIN_K", "0"))
     max_k = int(os.environ.get("SWEEP_MAX_K", "10"))
     ops = os.environ.get("SWEEP_OPS", "allreduce,reduce_scatter_rank,reduce_scatter_ring,allgather,broadcast")
     algos = os.environ.get("SWEEP_ALGOS", "fused,ring_steps,persistent,rd,rab,tree").split(",")
     tree_codes = {"rd": D.DDP_ALGO_RECURSIVE_DOUBLING, "rab": D.DDP_ALGO_RABENSEIFNER, "tree": D.DDP_ALGO_TREE}
     reps = int(os.environ.get("SWEEP_REPS", "20"))
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    batches = int(os.environ.get("SWEEP_BATCHES", "5"))
+    wflush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    rflush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    rotate_budget = 4 << 30
+
+    def flush():
+        wflush.fill_(1)
+        rflush.sum()
+
     for p in ps:
-        for k in range(max_k + 1):
+        for k in range(min_k, max_k + 1):
             M = 1024 * 4 ** k
             if p * M > 64 << 30:
                 continue
             n = M // 4
-            bufs = []
-            for r in range(p):
-                t = torch.empty(n, dtype=torch.float32, device="cuda")
-                synth.fill_(t, "uniform", 1005, r)
-                bufs.append(t)
             m = n // p
-            outs = [torch.empty(max(n, p * m), dtype=torch.float32, device="cuda") for _ in range(p)] \
-                if ops != "allreduce" else []
+            with_outs = ops != "allreduce"
+            out_elems = max(n, p * m)
+            set_bytes = p * M + (p * out_elems * 4 if with_outs else 0)
+            nsets = 1
+            if set_bytes < 2 * l2:
+                nsets = max(1, min(reps, rotate_budget // set_bytes))
+            sets = []
+            for _ in range(nsets):
+                bufs = []
+                for r in range(p):
+                    t = torch.empty(n, dtype=torch.float32, device="cuda")
+                    synth.fill_(t, "uniform", 1005, r)
+                    bufs.append(t)
+                outs = [torch.empty(out_elems, dtype=torch.float32, device="cuda") for _ in range(p)] \
+                    if with_outs else []
+                sets.append((bufs, outs))
             for op in ops.split(","):
                 for an in algos:
                     if an in ("persistent", "rd", "rab", "tree") and op != "allreduce":
                         continue
                     al = tree_codes[an] if an in tree_codes else (algo_code(an) if an != "persistent" else None)
-                    if op == "allreduce" and an == "persistent":
-                        fn = lambda: D.ddp_allreduce_persistent(bufs, n, D.DDP_FLOAT32, float(p))
-                        nbytes = 2 * p * M
-                    elif op == "allreduce":
-                        fn = lambda: D.ddp_allreduce(bufs, n, D.DDP_FLOAT32, float(p), al)
-                        nbytes = 2 * p * M
-                    elif op.startswith("reduce_scatter"):
-                        own = D.DDP_OWN_RANK if op.endswith("rank") else D.DDP_OWN_RING
-                        fn = lambda: D.ddp_reduce_scatter(bufs, outs, n, D.DDP_FLOAT32, 1.0, own, al)
-                        nbytes = p * M + M
-                    elif op == "allgather":
-                        fn = lambda: D.ddp_allgather(bufs, outs, m, D.DDP_FLOAT32, D.DDP_OWN_RANK, al)
-                        nbytes = M + p * M
-                    else:
-                        fn = lambda: D.ddp_broadcast(bufs, M, 0, al)
-                        nbytes = p * M
-                    small = nbytes < 2 * l2
-                    for _ in range(3):
-                        fn()
-                    times = []
-                    for _ in range(reps):
-                        if small:
-                            flush.fill_(1)
-                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                        a.record()
-                        fn()
-                        b.record()
-                        b.synchronize()
-                        times.append(a.elapsed_time(b))
-                    t = statistics.median(times) / 1e3
+
+                    def call(i, op=op, an=an, al=al):
+                        bufs, outs = sets[i % nsets]
+                        if op == "allreduce" and an == "persistent":
+                            D.ddp_allreduce_persistent(bufs, n, D.DDP_FLOAT32, float(p))
+                        elif op == "allreduce":
+                            D.ddp_allreduce(bufs, n, D.DDP_FLOAT32, float(p), al)
+                        elif op.startswith("reduce_scatter"):
+                            own = D.DDP_OWN_RANK if op.endswith("rank") else D.DDP_OWN_RING
+                            D.ddp_reduce_scatter(bufs, outs, n, D.DDP_FLOAT32, 1.0, own, al)
+                        elif op == "allgather":
+                            D.ddp_allgather(bufs, outs, m, D.DDP_FLOAT32, D.DDP_OWN_RANK, al)
+                        else:
+                            D.ddp_broadcast(bufs, M, 0, al)
+
+                    nbytes = {"allreduce": 2 * p * M, "allgather": M + p * M, "broadcast": p * M}.get(
+                        op, p * M + M)
+
+                    # warm-up (first-use lookups, workspace pools), then one timed
+                    # launch to size the batch: up to `reps` launches, fewer when
+                    # one launch is long (a batch of about 5 ms is enough there)
+                    for i in range(min(nsets, 3) + 1):
+                        call(i)
+                    flush()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    call(0)
+                    b.record()
+                    b.synchronize()
+                    t1 = a.elapsed_time(b) / 1e3
+                    nrep = max(3, min(reps, int(math.ceil(5e-3 / max(t1, 1e-9)))))
+                    nbat = batches if t1 < 1e-3 else 3
+
+                    def batch(nrep=nrep):
+                        for i in range(nrep):
+                            call(i)
+
+                    def timed(run, nrep=nrep, nbat=nbat):
+                        out = []
+                        for _ in range(nbat):
+                            flush()
+                            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                            a.record()
+                            run()
+                            b.record()
+                            b.synchronize()
+                            out.append(a.elapsed_time(b) / 1e3 / nrep)
+                        return statistics.median(out)
+
+                    t_eager = timed(batch)
+                    t_graph = None
+                    if an != "persistent":
+                        g = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(g):
+                            batch()
+                        g.replay()
+                        torch.cuda.synchronize()
+                        t_graph = timed(g.replay)
+                        del g
+                    t = t_graph if t_graph is not None else t_eager
                     gbs = nbytes / t / 1e9
                     line = {"sweep": op, "algo": an, "p": p, "bytes": M, "us": round(t * 1e6, 2),
+                            "us_eager": round(t_eager * 1e6, 2), "timing": "graph" if t_graph else "eager",
                             "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
                             "busbw_gbs": round(M / t / 1e9 * 2 * (p - 1) / p, 1) if op == "allreduce" else None,
-                            "l2_flushed": small}
+                            "input_copies": nsets, "reps": nrep, "batches": nbat}
                     print(json.dumps(line), flush=True)
-            del bufs, outs
+            del sets
             torch.cuda.empty_cache()
 
 

@@ -205,9 +205,11 @@ struct SegCopyArgs {
 };
 
 // Multi-tensor fan-out (coalesced broadcast): tensor t goes from src[t] to
-// dst[t * ndst + q] for q < ndst.
-constexpr int kFanT = 64;
-constexpr int kFanD = 1024;
+// dst[t * ndst + q] for q < ndst. Sized so that a whole model's buffer set
+// (ResNet-50 has 159 BN buffers) goes out in one launch at p = 8; the struct
+// (about 21 KB) stays inside the 32 KB kernel-parameter limit.
+constexpr int kFanT = 256;
+constexpr int kFanD = 2048;
 struct MultiFanoutArgs {
   const char* src[kFanT];
   int64_t bytes[kFanT];
@@ -215,5 +217,6 @@ struct MultiFanoutArgs {
   char* dst[kFanD];
   int ntensors, ndst;
 };
+static_assert(sizeof(MultiFanoutArgs) <= 32764, "kernel parameters are limited to 32764 bytes");
 
 }  // namespace ddp

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) k_multi_fanout(const __grid_constant
   const int64_t b0 = static_cast<int64_t>(b - a.tile0[t]) * kTileBytes;
   const int64_t len = min(kTileBytes, a.bytes[t] - b0);
   if (len <= 0) return;
-  __shared__ char* dst[kFanD];
+  __shared__ char* dst[kMaxP];  // ndst <= p - 1
   for (int q = threadIdx.x; q < a.ndst; q += blockDim.x) dst[q] = a.dst[t * a.ndst + q] + b0;
   __syncthreads();
   copy_to_all(a.src[t] + b0, dst, a.ndst, len, threadIdx.x, blockDim.x);

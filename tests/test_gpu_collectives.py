@@ -175,6 +175,27 @@ def test_broadcast_coalesced_mixed_dtypes_and_roots(algo):
             assert np.array_equal(tensors[r][j].cpu().reshape(-1).numpy().view(np.uint8), want[r][j])
 
 
+@pytest.mark.parametrize("k,launches", [(159, 1), (600, 3)])
+def test_fused_coalesced_broadcast_launch_split(k, launches):
+    """The fused coalesced broadcast packs up to 256 tensors (at p = 8) into
+    one launch: the ResNet-50 buffer count fits one; 600 tensors of odd byte
+    sizes split across three, with every byte still the root's."""
+    p, root = 8, 2
+    rng = np.random.default_rng(k)
+    sizes = [int(x) for x in rng.integers(1, 3000, size=k)]
+    tensors = [[torch.full((s,), r * 7 + j % 5, dtype=torch.uint8, device="cuda") for j, s in enumerate(sizes)]
+               for r in range(p)]
+    host = [[t.cpu().numpy().copy() for t in row] for row in tensors]
+    before = D.ddp_kernel_launches()
+    D.ddp_broadcast_coalesced(tensors, sizes, root, 0, D.DDP_ALGO_FUSED)
+    assert D.ddp_kernel_launches() - before == launches
+    want, _ = orc.broadcast_coalesced(host, root, 250 * 1024 * 1024)
+    for r in range(p):
+        for j in range(k):
+            assert np.array_equal(tensors[r][j].cpu().numpy(), want[r][j]), (r, j)
+    _no_device_error()
+
+
 def test_zero_sizes_are_noops():
     devs, hosts, _ = make_replicas(4, 16, "f32")
     D.ddp_allreduce(devs, 0, D.DDP_FLOAT32, 4.0)
