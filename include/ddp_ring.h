@@ -67,8 +67,10 @@ typedef enum {
                                asynchronous copies (falls back to the register path
                                when p > 64 or the replicas' alignments differ)      */
   /* Tree-shaped literal all-reduces ([DP] "Latency, trees, and choosing an
-   * algorithm"; [COLL] tree all-reduce). ddp_allreduce only; fp32 only
-   * (DDP_ERR_DTYPE otherwise); the pairwise tree order, not the ring's. */
+   * algorithm"; [COLL] tree all-reduce). ddp_allreduce only; the pairwise
+   * tree order, not the ring's. bf16 buffers are widened into a stream-ordered
+   * fp32 workspace of p * n floats, reduced there and rounded once at the end
+   * (one launch more on each side; DDP_ERR_NOMEM if the workspace fails). */
   DDP_ALGO_RECURSIVE_DOUBLING = 4, /* log2 p steps: pairs r, r^2^j swap and add; p = 2^k */
   DDP_ALGO_RABENSEIFNER = 5,       /* recursive halving (keep lower half if bit d clear),
                                       then recursive doubling of owned chunks; p = 2^k */
@@ -200,7 +202,10 @@ ddp_status ddp_allreduce_ex(void* const* bufs, int32_t p, int64_t n, ddp_dtype d
  * injection. [COLL] "Ring allreduce in two passes" (rank r receives from
  * r - 1 each step) and its exercise on a configurable receive timeout that
  * surfaces a deadline error instead of waiting forever.
- * Same result as ddp_allreduce, bit for bit (fp32 only, else DDP_ERR_DTYPE).
+ * Same result as ddp_allreduce, bit for bit. bf16 buffers are widened into a
+ * stream-ordered fp32 workspace of p * n floats, the ring runs there and each
+ * finished value is rounded to bf16 once (DDP_ERR_NOMEM if the workspace
+ * cannot be had); after a wait ran out their contents are unspecified.
  * Each simulated rank gets blocks of its own; receiver d waits, before step t,
  * until its sender d-1 has posted t steps. A wait gives up after timeout_ns
  * (0 means 1 s); the kernel then records the failure and ends (no trap).

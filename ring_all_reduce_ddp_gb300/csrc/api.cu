@@ -633,16 +633,53 @@ ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtyp
                          ddp_algo algo, cudaStream_t stream) {
   if (is_tree_algo(algo)) {
     DDP_TRY(check_common(p, n, dtype));
-    DDP_CHECK(dtype == DDP_FLOAT32, DDP_ERR_DTYPE, "the tree-shaped all-reduces run fp32 buffers");
     DDP_TRY(check_divisor(divisor));
     DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
+    const int es = esize(dtype);
     std::vector<std::pair<uintptr_t, uintptr_t>> rg;
-    for (int r = 0; r < p; ++r) rg.push_back(range_of(bufs[r], n * 4));
+    for (int r = 0; r < p; ++r) rg.push_back(range_of(bufs[r], n * es));
     DDP_CHECK(disjoint(rg), DDP_ERR_ARG, "replica buffers overlap");
     if (n == 0) return DDP_OK;
+    if (algo != DDP_ALGO_TREE) {
+      const bool pow2 = (p & (p - 1)) == 0;
+      DDP_CHECK(pow2, DDP_ERR_ARG, "recursive doubling and Rabenseifner need p a power of two");
+    }
     std::vector<float*> B(p);
-    for (int r = 0; r < p; ++r) B[r] = static_cast<float*>(bufs[r]);
-    return run_tree_allreduce(B.data(), p, n, divisor, algo, stream);
+    if (dtype == DDP_FLOAT32) {
+      for (int r = 0; r < p; ++r) B[r] = static_cast<float*>(bufs[r]);
+      return run_tree_allreduce(B.data(), p, n, divisor, algo, stream);
+    }
+    if (p == 1)
+      return run_fused(const_cast<const void* const*>(bufs), bufs, 1, n, dtype, divisor, false, 0, false, stream);
+    // bf16: the schedule runs on fp32 partials (widened exactly), and each
+    // replica's finished fp32 value is rounded to bf16 once at the end.
+    const int64_t slot = (n * 4 + 255) / 256 * 256;
+    void* wsv = nullptr;
+    const cudaError_t ea = cudaMallocAsync(&wsv, slot * p, stream);
+    if (ea != cudaSuccess) {
+      (void)cudaGetLastError();  // an allocation failure is not sticky: do not let a later launch report it
+      return fail(DDP_ERR_NOMEM, std::string("tree workspace: ") + cudaGetErrorString(ea));
+    }
+    char* ws = static_cast<char*>(wsv);
+    for (int r = 0; r < p; ++r) B[r] = reinterpret_cast<float*>(ws + slot * r);
+    ConvertArgs cv;
+    std::memset(&cv, 0, sizeof(cv));
+    cv.n = n;
+    cv.njobs = p;
+    for (int r = 0; r < p; ++r) { cv.src[r] = bufs[r]; cv.dst[r] = B[r]; }
+    cudaError_t e = launch_convert(cv, stream);
+    ddp_status rc = e == cudaSuccess ? run_tree_allreduce(B.data(), p, n, divisor, algo, stream)
+                                     : cuda_fail(e, "widen launch");
+    if (rc == DDP_OK) {
+      cv.to_bf16 = 1;
+      for (int r = 0; r < p; ++r) { cv.src[r] = B[r]; cv.dst[r] = bufs[r]; }
+      e = launch_convert(cv, stream);
+      if (e != cudaSuccess) rc = cuda_fail(e, "narrow launch");
+    }
+    const cudaError_t ef = cudaFreeAsync(wsv, stream);
+    if (rc != DDP_OK) return rc;
+    if (ef != cudaSuccess) return cuda_fail(ef, "tree workspace release");
+    return DDP_OK;
   }
   return ddp_allreduce_ex(bufs, p, n, dtype, divisor, algo, 0u, stream);
 }
@@ -1258,7 +1295,6 @@ ddp_status ddp_allreduce_persistent(void* const* bufs, int32_t p, int64_t n, ddp
                                     int64_t timeout_ns, int32_t fault_rank, int32_t fault_step, int32_t* status,
                                     cudaStream_t stream) {
   DDP_TRY(check_common(p, n, dtype));
-  DDP_CHECK(dtype == DDP_FLOAT32, DDP_ERR_DTYPE, "the persistent ring runs fp32 buffers");
   DDP_TRY(check_divisor(divisor));
   DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
   DDP_CHECK(timeout_ns >= 0, DDP_ERR_ARG, "timeout_ns must be >= 0");
@@ -1266,7 +1302,7 @@ ddp_status ddp_allreduce_persistent(void* const* bufs, int32_t p, int64_t n, ddp
   DDP_CHECK(fault_rank == -1 || (fault_rank >= 0 && fault_rank < p && fault_step >= 0 && fault_step < T),
             DDP_ERR_ARG, "fault_rank must be -1 or a rank, fault_step a step in [0, 2(p-1))");
   std::vector<std::pair<uintptr_t, uintptr_t>> rg;
-  for (int r = 0; r < p; ++r) rg.push_back(range_of(bufs[r], n * 4));
+  for (int r = 0; r < p; ++r) rg.push_back(range_of(bufs[r], n * esize(dtype)));
   DDP_CHECK(disjoint(rg), DDP_ERR_ARG, "replica buffers overlap");
   if (status) DDP_CUDA(cudaMemsetAsync(status, 0, 4 * sizeof(int32_t), stream), "status reset");
   if (n == 0) return DDP_OK;
@@ -1274,6 +1310,42 @@ ddp_status ddp_allreduce_persistent(void* const* bufs, int32_t p, int64_t n, ddp
                                stream);
   const int max_blocks = ring_persistent_max_blocks();
   DDP_CHECK(max_blocks >= p, DDP_ERR_ARG, "more ranks than co-resident blocks for the persistent ring");
+  if (dtype == DDP_BFLOAT16) {
+    // fp32 partials for the whole ring (reading A10): widen into a workspace,
+    // run the fp32 ring there, round each finished value to bf16 once.
+    const int64_t slot = (n * 4 + 255) / 256 * 256;
+    void* wsv = nullptr;
+    const cudaError_t ea = cudaMallocAsync(&wsv, slot * p, stream);
+    if (ea != cudaSuccess) {
+      (void)cudaGetLastError();  // an allocation failure is not sticky: do not let a later launch report it
+      return fail(DDP_ERR_NOMEM, std::string("persistent ring workspace: ") + cudaGetErrorString(ea));
+    }
+    std::vector<void*> W(p);
+    ConvertArgs cv;
+    std::memset(&cv, 0, sizeof(cv));
+    cv.n = n;
+    cv.njobs = p;
+    for (int r = 0; r < p; ++r) {
+      W[r] = static_cast<char*>(wsv) + slot * r;
+      cv.src[r] = bufs[r];
+      cv.dst[r] = W[r];
+    }
+    cudaError_t e = launch_convert(cv, stream);
+    ddp_status rc = e == cudaSuccess
+                        ? ddp_allreduce_persistent(W.data(), p, n, DDP_FLOAT32, divisor, timeout_ns, fault_rank,
+                                                   fault_step, status, stream)
+                        : cuda_fail(e, "widen launch");
+    if (rc == DDP_OK) {
+      cv.to_bf16 = 1;
+      for (int r = 0; r < p; ++r) { cv.src[r] = W[r]; cv.dst[r] = bufs[r]; }
+      e = launch_convert(cv, stream);
+      if (e != cudaSuccess) rc = cuda_fail(e, "narrow launch");
+    }
+    const cudaError_t ef = cudaFreeAsync(wsv, stream);
+    if (rc != DDP_OK) return rc;
+    if (ef != cudaSuccess) return cuda_fail(ef, "persistent ring workspace release");
+    return DDP_OK;
+  }
   const int64_t cs = chunk_size(n, p);
   int B = max_blocks / p;
   const int64_t useful = std::max<int64_t>(1, (cs + kThreads * 4 - 1) / (kThreads * 4));

@@ -181,6 +181,17 @@ struct PairCopyArgs {
   int njobs;
 };
 
+// Precision change of p buffers of n elements each: job j converts src[j]
+// into dst[j]; to_bf16 = 0 widens bf16 to fp32 (exact), 1 narrows fp32 to
+// bf16 (round to nearest even).
+struct ConvertArgs {
+  const void* src[kMaxP];
+  void* dst[kMaxP];
+  int64_t n;
+  int njobs;
+  int to_bf16;
+};
+
 // Fan-out: job j copies nbytes from src[j] to every dst[q] + job_off[j].
 struct FanoutArgs {
   const char* src[kMaxP];

@@ -136,6 +136,42 @@ __global__ void __launch_bounds__(kThreads) k_multi_fanout(const __grid_constant
   copy_to_all(a.src[t] + b0, dst, a.ndst, len, threadIdx.x, blockDim.x);
 }
 
+// One job per blockIdx.y. Eight elements per thread and step (16 bytes of
+// bf16, 32 of fp32) when the bf16 side is 16-byte aligned and the fp32 side
+// 32-byte aligned; the rest element by element.
+__global__ void __launch_bounds__(kThreads) k_convert(const __grid_constant__ ConvertArgs a) {
+  const int j = blockIdx.y;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const uintptr_t bf = reinterpret_cast<uintptr_t>(a.to_bf16 ? a.dst[j] : a.src[j]);
+  const uintptr_t f32 = reinterpret_cast<uintptr_t>(a.to_bf16 ? a.src[j] : a.dst[j]);
+  const int64_t nv = (bf % 16 == 0 && f32 % 32 == 0) ? a.n / 8 : 0;
+  if (a.to_bf16) {
+    const float4* s = static_cast<const float4*>(a.src[j]);
+    uint4* d = static_cast<uint4*>(a.dst[j]);
+    for (int64_t v = tid; v < nv; v += stride) {
+      const float4 x = s[2 * v], y = s[2 * v + 1];
+      const float f[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+      d[v] = Vec<__nv_bfloat16>::pack(f);
+    }
+    const float* ss = static_cast<const float*>(a.src[j]);
+    __nv_bfloat16* dd = static_cast<__nv_bfloat16*>(a.dst[j]);
+    for (int64_t i = nv * 8 + tid; i < a.n; i += stride) dd[i] = narrow<__nv_bfloat16>(ss[i]);
+  } else {
+    const uint4* s = static_cast<const uint4*>(a.src[j]);
+    float4* d = static_cast<float4*>(a.dst[j]);
+    for (int64_t v = tid; v < nv; v += stride) {
+      float f[8];
+      Vec<__nv_bfloat16>::unpack(s[v], f);
+      d[2 * v] = make_float4(f[0], f[1], f[2], f[3]);
+      d[2 * v + 1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    const __nv_bfloat16* ss = static_cast<const __nv_bfloat16*>(a.src[j]);
+    float* dd = static_cast<float*>(a.dst[j]);
+    for (int64_t i = nv * 8 + tid; i < a.n; i += stride) dd[i] = widen(ss[i]);
+  }
+}
+
 int grid_x_for(int64_t tiles, int rows) {
   const int64_t target = static_cast<int64_t>(sm_count()) * (2048 / kThreads);
   int64_t bx = (target + rows - 1) / rows;
@@ -170,6 +206,14 @@ cudaError_t launch_seg_copy(const SegCopyArgs& a, ddp_dtype dt, cudaStream_t s) 
   if (a.nseg <= 0 || ntiles <= 0) return cudaSuccess;
   if (dt == DDP_BFLOAT16) k_seg_copy<__nv_bfloat16><<<ntiles, kThreads, 0, s>>>(a);
   else k_seg_copy<float><<<ntiles, kThreads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t s) {
+  if (a.njobs <= 0 || a.n <= 0) return cudaSuccess;
+  const dim3 grid(grid_x_for((a.n + 8 * kThreads - 1) / (8 * kThreads), a.njobs), a.njobs);
+  k_convert<<<grid, kThreads, 0, s>>>(a);
   count_launch();
   return cudaGetLastError();
 }

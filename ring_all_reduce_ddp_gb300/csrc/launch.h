@@ -23,6 +23,7 @@ cudaError_t launch_pair_add(const PairAddArgs& a, cudaStream_t s);
 cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s);
 cudaError_t launch_seg_copy(const SegCopyArgs& a, ddp_dtype dt, cudaStream_t s);
 cudaError_t launch_multi_fanout(const MultiFanoutArgs& a, cudaStream_t s);
+cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t s);
 
 // Synchronize s, then read and clear the device error word.
 cudaError_t read_device_error(cudaStream_t s, int* code);

@@ -65,11 +65,39 @@ def test_injected_fault_is_detected_and_the_context_survives(p, fault_rank, faul
         assert_bit_equal(to_host(devs2[r]), want[r])
 
 
+@pytest.mark.parametrize("p,n", [(1, 999), (2, 4099), (4, 277421), (8, 65536 * 3 + 5), (16, 100003)])
+def test_persistent_ring_in_bf16_rounds_once(p, n):
+    """bf16 replicas: the ring runs on fp32 partials in a workspace and each
+    finished value is rounded once, so the bits equal the literal ring's."""
+    devs, hosts, _ = make_replicas(p, n, "bf16", "normal", seed=970 + p)
+    status = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+    before = D.ddp_kernel_launches()
+    D.ddp_allreduce_persistent(devs, n, D.DDP_BFLOAT16, float(p), LIMIT_NS, -1, 0, status)
+    launched = D.ddp_kernel_launches() - before
+    torch.cuda.synchronize()
+    want, _ = orc.allreduce(hosts, n, float(p), "bf16")
+    for r in range(p):
+        assert_bit_equal(to_host(devs[r]), want[r], f"replica {r}")
+    assert status.cpu().tolist() == [0, 0, 0, 0]
+    assert launched == (3 if p > 1 else 1)  # widen, the ring, narrow
+    assert D.ddp_device_error() == 0
+
+
+def test_bf16_persistent_ring_reports_an_injected_fault():
+    p, n = 4, 40000 * 4 + 3
+    devs, _, _ = make_replicas(p, n, "bf16", "uniform", seed=980)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    D.ddp_allreduce_persistent(devs, n, D.DDP_BFLOAT16, 1.0, LIMIT_NS, 1, 2, status)
+    torch.cuda.synchronize()
+    code, rank, step, gave_up = status.cpu().tolist()
+    assert code == D.DDP_ERR_TIMEOUT and gave_up >= 1
+    j = (rank - 1) % p
+    assert j >= 1 and step == min(2 + j, 2 * (p - 1))
+    assert D.ddp_device_error() == 2
+    assert D.ddp_device_error() == 0
+
+
 def test_persistent_ring_rejects_bad_arguments():
-    devs, _, _ = make_replicas(4, 100, "bf16")
-    with pytest.raises(D.DDPError) as e:
-        D.ddp_allreduce_persistent(devs, 100, D.DDP_BFLOAT16, 1.0)
-    assert e.value.status == D.DDP_ERR_DTYPE
     devs, _, _ = make_replicas(4, 100, "f32")
     with pytest.raises(D.DDPError) as e:
         D.ddp_allreduce_persistent(devs, 100, D.DDP_FLOAT32, 1.0, 0, 4, 0)

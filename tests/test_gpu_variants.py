@@ -112,7 +112,43 @@ def test_tree_algos_reject_what_they_cannot_do():
         with pytest.raises(D.DDPError) as e:
             D.ddp_allreduce(devs, 100, D.DDP_FLOAT32, 1.0, algo)
         assert e.value.status == D.DDP_ERR_ARG
-    devs, _, _ = make_replicas(4, 100, "bf16")
-    with pytest.raises(D.DDPError) as e:
-        D.ddp_allreduce(devs, 100, D.DDP_BFLOAT16, 1.0, D.DDP_ALGO_TREE)
-    assert e.value.status == D.DDP_ERR_DTYPE
+    devs, _, _ = make_replicas(6, 100, "bf16")
+    for algo in (D.DDP_ALGO_RECURSIVE_DOUBLING, D.DDP_ALGO_RABENSEIFNER):
+        with pytest.raises(D.DDPError) as e:
+            D.ddp_allreduce(devs, 100, D.DDP_BFLOAT16, 1.0, algo)
+        assert e.value.status == D.DDP_ERR_ARG
+
+
+@pytest.mark.parametrize("name", ["rd", "rab", "tree"])
+@pytest.mark.parametrize("p,n", [(1, 77), (2, 4099), (4, 3), (8, 65536 * 3 + 5), (16, 100003)])
+def test_trees_in_bf16_round_once(name, p, n):
+    """bf16 replicas: fp32 partials through the whole schedule, one rounding
+    of each finished value; the bits equal the oracle's."""
+    algo, ref = TREE[name]
+    devs, hosts, _ = make_replicas(p, n, "bf16", "normal", seed=1300 + p)
+    before = D.ddp_kernel_launches()
+    D.ddp_allreduce(devs, n, D.DDP_BFLOAT16, float(p), algo)
+    launched = D.ddp_kernel_launches() - before
+    want, info = ref(hosts, n, float(p), "bf16")
+    for r in range(p):
+        assert_bit_equal(to_host(devs[r]), want[r], f"replica {r}")
+    if p > 1:
+        assert launched == info["steps"] + 2  # widen, the schedule's steps, narrow
+    assert D.ddp_device_error() == 0
+
+
+def test_tree_bf16_on_unaligned_replicas():
+    """Replicas at odd element offsets take the element-by-element widen and
+    narrow; the result is the same and nothing outside the replicas changes."""
+    p, n = 4, 5003
+    algo, ref = TREE["tree"]
+    offs = [1, 3, 0, 5]
+    devs, hosts, bases = make_replicas(p, n, "bf16", "uniform", seed=1400, offsets=offs)
+    before = [to_host(b).copy() for b in bases]
+    D.ddp_allreduce(devs, n, D.DDP_BFLOAT16, 3.0, algo)
+    want, _ = ref(hosts, n, 3.0, "bf16")
+    for r in range(p):
+        assert_bit_equal(to_host(devs[r]), want[r], f"replica {r}")
+        after = to_host(bases[r])
+        assert np.array_equal(after[:offs[r]], before[r][:offs[r]])
+        assert np.array_equal(after[offs[r] + n:], before[r][offs[r] + n:])
