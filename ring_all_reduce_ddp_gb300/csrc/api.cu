@@ -459,7 +459,7 @@ ddp_status plan_bucket_launches(int32_t p, int32_t k, const void* const* grads, 
   for (int32_t j = 0; j < k; ++j) n = std::max(n, offset[j] + numel[j]);
   if (n == 0) return DDP_OK;
   const int64_t cs = chunk_size(n, p);
-  const int64_t tile = kBucketTileBytes / esize(dt);
+  const int64_t tile = bucket_tile_elems(esize(dt));
   const int slots_per_launch = kBucketPtrs / p;
   DDP_CHECK(slots_per_launch >= 1, DDP_ERR_ARG, "too many replicas for the in-place bucket kernel");
   BucketArgs a;
@@ -1004,7 +1004,7 @@ cudaError_t reducer_free_device(ddp_reducer* h) {
 // origin each), in bucket order, and upload the table to device memory once.
 ddp_status build_reducer_table(ddp_reducer* h) {
   const int p = h->p;
-  const int64_t tile = kBucketTileBytes / esize(h->dt);
+  const int64_t tile = bucket_tile_elems(esize(h->dt));
   std::vector<void*> ptr;
   std::vector<int64_t> start, len;
   std::vector<int32_t> slot, origin, tile0{0};

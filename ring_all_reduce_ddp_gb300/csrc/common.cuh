@@ -106,10 +106,17 @@ struct StagedArgs {
 // the intersections of its tensors with its chunks, so each piece has one
 // summation origin (its chunk index). ptr[slot * p + r] is replica r's tensor
 // in local slot `slot`; piece i covers elements [start, start + len) of that
-// tensor; tile0 is the prefix of each piece's tiles of kBucketTile elements.
+// tensor; tile0 is the prefix of each piece's tiles of bucket_tile_elems
+// elements. Tile bytes per replica, measured on GB300 over the ResNet-50,
+// GPT-2 and Llama-1B-shaped gradient sets: 16 KB for fp32 (8 and 32 KB were
+// slower), 64 KB for bf16 (1 % faster than 16 KB).
 constexpr int kBucketPtrs = 1024;
 constexpr int kBucketPieces = 256;
 constexpr int kBucketTileBytes = 16384;
+constexpr int kBucketTileBytesBf16 = 65536;
+__host__ __device__ constexpr int64_t bucket_tile_elems(int elem_size) {
+  return elem_size == 2 ? kBucketTileBytesBf16 / 2 : kBucketTileBytes / elem_size;
+}
 struct BucketArgs {
   void* ptr[kBucketPtrs];
   int64_t start[kBucketPieces];

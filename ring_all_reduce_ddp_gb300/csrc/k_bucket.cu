@@ -11,7 +11,7 @@
 // ((x_c + x_{c+1}) + ...) + x_{c+p-1}, then divided once by the divisor: the
 // same bits as the ring on the flat bucket. Work is cut into pieces (a tensor
 // intersected with a chunk: one origin each) and pieces into tiles of
-// kBucketTileBytes per replica; a persistent grid strides over the tiles.
+// bucket_tile_elems elements per replica; a persistent grid strides over the tiles.
 #include <atomic>
 
 #include "launch.h"
@@ -41,7 +41,7 @@ __device__ __forceinline__ int find_piece(const int32_t* tile0, int n, int32_t b
 template <typename T, int P>
 __device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divisor) {
   constexpr int V = Vec<T>::N;
-  constexpr int64_t kTile = kBucketTileBytes / sizeof(T);
+  constexpr int64_t kTile = bucket_tile_elems(sizeof(T));
   const int p = (P > 0) ? P : a.p;
   const int i = find_piece(a.tile0, a.npieces, b);
   const int64_t t0 = a.start[i] + static_cast<int64_t>(b - a.tile0[i]) * kTile;  // first element of the tile
