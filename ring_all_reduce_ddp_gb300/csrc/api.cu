@@ -1358,9 +1358,9 @@ ddp_status ddp_allreduce_persistent(void* const* bufs, int32_t p, int64_t n, ddp
   a.timeout_ns = timeout_ns > 0 ? timeout_ns : 1000000000LL;
   a.status = status;
   void* flags = nullptr;
-  DDP_CUDA(cudaMallocAsync(&flags, static_cast<size_t>(p) * B * sizeof(int), stream), "step flags allocation");
+  DDP_CUDA(cudaMallocAsync(&flags, static_cast<size_t>(p) * B * kFlagStride * sizeof(int), stream), "step flags allocation");
   a.flags = static_cast<int*>(flags);
-  cudaError_t e = cudaMemsetAsync(flags, 0, static_cast<size_t>(p) * B * sizeof(int), stream);
+  cudaError_t e = cudaMemsetAsync(flags, 0, static_cast<size_t>(p) * B * kFlagStride * sizeof(int), stream);
   if (e == cudaSuccess) e = launch_ring_persistent(a, stream);
   const cudaError_t e2 = cudaFreeAsync(flags, stream);
   if (e != cudaSuccess) return cuda_fail(e, "persistent ring launch");

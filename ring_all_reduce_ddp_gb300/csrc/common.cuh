@@ -156,9 +156,10 @@ struct RingStepArgs {
 // Persistent literal ring (fp32, in place): every rank's blocks in one
 // cooperative launch; block b of rank d handles slice b of each step's chunk
 // and waits for block b of rank d-1 to have posted the previous step.
+constexpr int kFlagStride = 32;  // ints between two step flags: one 128-byte line each
 struct PersistArgs {
   void* buf[kMaxP];
-  int* flags;          // [p][blocks_per_rank]: steps posted; zero at launch
+  int* flags;          // [p][blocks_per_rank][kFlagStride]: steps posted (first int); zero at launch
   int* status;         // caller's 4 device words, or null: {code, rank, step, waits that gave up}
   int64_t n, cs;
   float divisor;

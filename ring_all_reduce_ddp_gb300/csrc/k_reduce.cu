@@ -504,6 +504,14 @@ __global__ void __launch_bounds__(kThreads) k_rs_step_ws(const __grid_constant__
 // the block stops, so its own successors time out after it and the kernel
 // ends. Data of other ranks is read through L2 (ld.global.cg): L1 is not
 // coherent across SMs.
+//
+// Each (rank, slice) flag has a 128-byte line of its own (kFlagStride ints):
+// with flags packed side by side, every posting store contended with the many
+// receivers polling the same line, which doubled the time per step at 1-4 MiB
+// buffers on GB300. A step is posted by bar.sync followed by one thread's
+// st.release.gpu: the release is cumulative over the block's writes ordered
+// before it by the barrier, so no separate fence is needed (an extra
+// fence.acq_rel cost 7-12 % of the step time).
 constexpr int kErrRingWait = 2;  // device error code: a ring step's wait ran out
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(kThreads) k_ring_persistent_f32(const __grid_c
   // (rank, need) and return false.
   auto wait_sender = [&](int need) -> bool {
     if (threadIdx.x == 0) {
-      const int* f = a.flags + snd * B + b;
+      const int* f = a.flags + (snd * B + b) * kFlagStride;
       int ok = 1;
       if (ld_acquire_gpu(f) < need) {
         const uint64_t t0 = global_ns();
@@ -606,10 +614,7 @@ __global__ void __launch_bounds__(kThreads) k_ring_persistent_f32(const __grid_c
       }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      st_release_gpu(a.flags + r * B + b, t + 1);
-    }
+    if (threadIdx.x == 0) st_release_gpu(a.flags + (r * B + b) * kFlagStride, t + 1);
   }
   // The sender's last step is read by no later step: wait for it too, so a
   // rank that stops before its final step is still caught.
