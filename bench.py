@@ -52,6 +52,7 @@ WORKLOAD_TEXT = {
 # ncu capture, as bytes per algorithmic byte; valid only while the kernel
 # source it was taken on is unchanged (checked by hash).
 NCU_TRAFFIC = {"kernel_sha256": "01d7a33ed28cf0197db3356be0cd7fb93067d84ba79f4a6c0ec8645c0d743f1a",
+               "config": "resnet50",  # the workload the capture ran; other workloads report null
                "dram_bytes_per_algorithmic_byte": (818.037504 + 757.198592) / 1635.650048}  # ncu: read + write MB per launch
 
 
@@ -338,7 +339,8 @@ def run_ours(args, ranks: Ranks):
     achieved = ab["allreduce"] * len(sync_ms) / (sum(sync_ms) / 1e3) / 1e9
     peak, peak_kind = peak_hbm()
     traffic = None
-    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]:
+    if (NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and NCU_TRAFFIC["config"] == args.config
+            and mode == D.DDP_SYNC_IN_PLACE and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]):
         traffic = int(NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * ab["allreduce"])
     bucket_mb = [round(n * esz / 2 ** 20, 2) for n in red.bucket_numel]
     kernel_name = ("k_bucket_allreduce_table: every bucket's flatten + ring-order all-reduce + unflatten "
@@ -347,20 +349,23 @@ def run_ours(args, ranks: Ranks):
 
     # End to end through the public API: every step copies every replica's
     # gradients in from pinned host memory, synchronises them and copies the
-    # result out. Two device copies of the workload alternate so that step i's
-    # copy-out (D2H stream) overlaps step i+1's copy-in (H2D stream); the sync
-    # runs on the compute stream between them.
-    grads_b, arenas_b = W.make_grads(cfg, f"cuda:{dev}")
-    red_b = Reducer(grads_b, cfg["first_cap"], cfg["cap"])
-    sets = [(arenas, red), (arenas_b, red_b)]
+    # result out. Three device copies of the workload rotate, so step i+1's
+    # copy-in (H2D stream) never waits for step i's sync: it only needs the
+    # copy-out of step i-2, long done. Both link directions stay busy; the
+    # sync runs on the compute stream between them.
+    NSETS = 3
+    sets = [(arenas, red)]
+    for _ in range(NSETS - 1):
+        g_x, a_x = W.make_grads(cfg, f"cuda:{dev}")
+        sets.append((a_x, Reducer(g_x, cfg["first_cap"], cfg["cap"])))
     host_in = [a.detach().to("cpu").pin_memory() for a in arenas]
     host_out = [torch.empty_like(h).pin_memory() for h in host_in]
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
-    h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [None, None]
+    h2d_done, comp_done, d2h_done = [ev() for _ in range(NSETS)], [ev() for _ in range(NSETS)], [None] * NSETS
 
     def e2e_step(i):
-        k = i % 2
+        k = i % NSETS
         ar_k, red_k = sets[k]
         with torch.cuda.stream(h2d_s):
             if d2h_done[k] is not None:
@@ -401,8 +406,8 @@ def run_ours(args, ranks: Ranks):
     e2e = {"value": round(step_bytes * k_e2e * ranks.world / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
            "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "ms_per_step": round(e2e_ms / k_e2e, 4),
            "steps": k_e2e,
-           "pipeline": "step i's copy-out overlaps step i+1's copy-in (two device copies, three streams)"}
-    del red_b, grads_b, arenas_b
+           "pipeline": "step i's copy-out overlaps step i+1's copy-in (three device copies, three streams)"}
+    del sets
 
     # the same step body (buffer broadcast + sync) captured once as a CUDA graph
     # and replayed: what host launch overhead costs the eager step

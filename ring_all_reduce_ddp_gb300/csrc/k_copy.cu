@@ -20,8 +20,15 @@ namespace {
 
 constexpr int kWordsInFlight = 4;
 constexpr int64_t kTileBytes = kSegTileBytes;  // = kThreads * 16 bytes * kWordsInFlight
+// The one-read, many-write fan-out: with more than kFanFewDst destinations it
+// keeps 2 words in flight per thread on 8 KB tiles, otherwise 4 on 16 KB.
+// Measured on GB300 (all-gather and broadcast, 1 MiB to 1 GiB): 2 words were
+// 2 to 4 % faster from 256 MiB at p = 8 and 64 and far faster at 1-4 MiB,
+// but 3 to 10 % slower with 1 to 4 destinations.
+constexpr int kFanFewDst = 4;
+template <int U> __host__ __device__ constexpr int64_t fan_tile_bytes() { return static_cast<int64_t>(kThreads) * 16 * U; }
 
-template <typename W>
+template <typename W, int U>
 __device__ __forceinline__ void copy_words(const char* s, char* const* d, int nd, int64_t nbytes,
                                            int tid, int nthr) {
   constexpr int64_t w = sizeof(W);
@@ -38,17 +45,17 @@ __device__ __forceinline__ void copy_words(const char* s, char* const* d, int nd
     for (int q = 0; q < nd; ++q) d[q][b] = v;
   }
   const W* sw = reinterpret_cast<const W*>(s + head);
-  for (int64_t k0 = tid; k0 < nw; k0 += static_cast<int64_t>(nthr) * kWordsInFlight) {
-    W v[kWordsInFlight];
+  for (int64_t k0 = tid; k0 < nw; k0 += static_cast<int64_t>(nthr) * U) {
+    W v[U];
 #pragma unroll
-    for (int u = 0; u < kWordsInFlight; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int64_t k = k0 + static_cast<int64_t>(u) * nthr;
       if (k < nw) v[u] = sw[k];
     }
     for (int q = 0; q < nd; ++q) {
       W* dw = reinterpret_cast<W*>(d[q] + head);
 #pragma unroll
-      for (int u = 0; u < kWordsInFlight; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int64_t k = k0 + static_cast<int64_t>(u) * nthr;
         if (k < nw) dw[k] = v[u];
       }
@@ -56,16 +63,18 @@ __device__ __forceinline__ void copy_words(const char* s, char* const* d, int nd
   }
 }
 
-// Copy nbytes from s to each of the nd destinations d[q] (one read, nd writes).
+// Copy nbytes from s to each of the nd destinations d[q] (one read, nd
+// writes), U words per thread in flight.
+template <int U = kWordsInFlight>
 __device__ __forceinline__ void copy_to_all(const char* s, char* const* d, int nd, int64_t nbytes,
                                             int tid, int nthr) {
   uintptr_t x = 0;
   for (int q = 0; q < nd; ++q) x |= reinterpret_cast<uintptr_t>(s) ^ reinterpret_cast<uintptr_t>(d[q]);
-  if ((x & 15) == 0) copy_words<uint4>(s, d, nd, nbytes, tid, nthr);
-  else if ((x & 7) == 0) copy_words<uint2>(s, d, nd, nbytes, tid, nthr);
-  else if ((x & 3) == 0) copy_words<uint32_t>(s, d, nd, nbytes, tid, nthr);
-  else if ((x & 1) == 0) copy_words<uint16_t>(s, d, nd, nbytes, tid, nthr);
-  else copy_words<uint8_t>(s, d, nd, nbytes, tid, nthr);
+  if ((x & 15) == 0) copy_words<uint4, U>(s, d, nd, nbytes, tid, nthr);
+  else if ((x & 7) == 0) copy_words<uint2, U>(s, d, nd, nbytes, tid, nthr);
+  else if ((x & 3) == 0) copy_words<uint32_t, U>(s, d, nd, nbytes, tid, nthr);
+  else if ((x & 1) == 0) copy_words<uint16_t, U>(s, d, nd, nbytes, tid, nthr);
+  else copy_words<uint8_t, U>(s, d, nd, nbytes, tid, nthr);
 }
 
 // ---------------------------------------------------------------- kernels
@@ -81,17 +90,19 @@ __global__ void __launch_bounds__(kThreads) k_pair_copy(const __grid_constant__ 
   }
 }
 
+template <int U>
 __global__ void __launch_bounds__(kThreads) k_fanout(const __grid_constant__ FanoutArgs a) {
+  constexpr int64_t kTile = fan_tile_bytes<U>();
   const int j = blockIdx.y;
-  const int64_t ntiles = (a.nbytes + kTileBytes - 1) / kTileBytes;
+  const int64_t ntiles = (a.nbytes + kTile - 1) / kTile;
   __shared__ char* dst[kMaxP];
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const int64_t b0 = t * kTileBytes;
-    const int64_t len = min(kTileBytes, a.nbytes - b0);
+    const int64_t b0 = t * kTile;
+    const int64_t len = min(kTile, a.nbytes - b0);
     __syncthreads();
     for (int q = threadIdx.x; q < a.ndst; q += blockDim.x) dst[q] = a.dst[q] + a.job_off[j] + b0;
     __syncthreads();
-    copy_to_all(a.src[j] + b0, dst, a.ndst, len, threadIdx.x, blockDim.x);
+    copy_to_all<U>(a.src[j] + b0, dst, a.ndst, len, threadIdx.x, blockDim.x);
   }
 }
 
@@ -195,8 +206,13 @@ cudaError_t launch_pair_copy(const PairCopyArgs& a, cudaStream_t s) {
 
 cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s) {
   if (a.njobs <= 0 || a.nbytes <= 0 || a.ndst <= 0) return cudaSuccess;
-  const dim3 grid(grid_x_for((a.nbytes + kTileBytes - 1) / kTileBytes, a.njobs), a.njobs);
-  k_fanout<<<grid, kThreads, 0, s>>>(a);
+  if (a.ndst <= kFanFewDst) {
+    constexpr int64_t t = fan_tile_bytes<4>();
+    k_fanout<4><<<dim3(grid_x_for((a.nbytes + t - 1) / t, a.njobs), a.njobs), kThreads, 0, s>>>(a);
+  } else {
+    constexpr int64_t t = fan_tile_bytes<2>();
+    k_fanout<2><<<dim3(grid_x_for((a.nbytes + t - 1) / t, a.njobs), a.njobs), kThreads, 0, s>>>(a);
+  }
   count_launch();
   return cudaGetLastError();
 }
