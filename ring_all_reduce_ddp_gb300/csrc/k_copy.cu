@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(kThreads) k_seg_copy(const __grid_constant__ S
 }
 
 __global__ void __launch_bounds__(kThreads) k_multi_fanout(const __grid_constant__ MultiFanoutArgs a) {
+  // a programmatic dependent (the Reducer's sync) may start its prologue now;
+  // it still waits for this grid to finish before it touches memory
+  asm volatile("griddepcontrol.launch_dependents;");
   const int32_t b = blockIdx.x;
   const int t = find_tile_owner(a.tile0, a.ntensors, b);
   const int64_t b0 = static_cast<int64_t>(b - a.tile0[t]) * kTileBytes;
