@@ -26,7 +26,10 @@
  *     DDP_ERR_CUDA. ddp_last_error() gives this thread's last message.
  *   - Replica buffers of one call must be distinct and must not overlap.
  *     Alignment is not required; misaligned heads and tails take a scalar path.
- *   - 1 <= p <= DDP_MAX_P. n == 0 (or nbytes == 0) is a no-op returning DDP_OK.
+ *   - 1 <= p <= DDP_MAX_P. n == 0 (or nbytes == 0) is a no-op returning DDP_OK
+ *     once the scalar arguments are valid; the buffer pointers are then not
+ *     read and may be NULL (an empty tensor has no storage). A ddp_ring
+ *     handle of n == 0 (zero steps) still needs non-NULL pointer arrays.
  *   - Floating point: the sum of p contributions is accumulated in fp32 in
  *     ring order, by IEEE round-to-nearest additions (no FMA contraction, no
  *     reassociation); the scale is one IEEE division; bf16 results are

@@ -10,6 +10,8 @@
 #include <utility>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "launch.h"
 
 using namespace ddp;
@@ -17,6 +19,17 @@ using namespace ddp;
 namespace {
 
 thread_local std::string t_error;
+
+// One NVTX range per C-ABI call that enqueues device work, named after the
+// entry point, for timeline tools and ncu's --nvtx filters. Without a tool
+// attached a range costs a pointer check.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define DDP_NVTX(name) NvtxRange nvtx_range_(name)
 
 ddp_status fail(ddp_status s, const std::string& msg) {
   t_error = msg;
@@ -603,6 +616,7 @@ ddp_status ddp_bucket_assign_order(int32_t k, const int64_t* numel, int32_t elem
 ddp_status ddp_bucket_flatten(int32_t p, int32_t k, const void* const* grads, const int64_t* numel,
                               const int64_t* offset, void* const* bucket, ddp_dtype dtype,
                               float predivide, cudaStream_t stream) {
+  DDP_NVTX("ddp_bucket_flatten");
   DDP_TRY(check_bucket_args(p, k, numel, offset, dtype));
   DDP_TRY(check_divisor(predivide));
   const int es = esize(dtype);
@@ -618,6 +632,7 @@ ddp_status ddp_bucket_flatten(int32_t p, int32_t k, const void* const* grads, co
 ddp_status ddp_bucket_unflatten(int32_t p, int32_t k, const void* const* bucket, const int64_t* numel,
                                 const int64_t* offset, void* const* grads, ddp_dtype dtype,
                                 cudaStream_t stream) {
+  DDP_NVTX("ddp_bucket_unflatten");
   DDP_TRY(check_bucket_args(p, k, numel, offset, dtype));
   const int es = esize(dtype);
   DDP_TRY(check_bucket_layout(p, k, const_cast<const void* const*>(grads), numel, offset, bucket, es));
@@ -631,9 +646,11 @@ ddp_status ddp_bucket_unflatten(int32_t p, int32_t k, const void* const* bucket,
 
 ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
                          ddp_algo algo, cudaStream_t stream) {
+  DDP_NVTX("ddp_allreduce");
   if (is_tree_algo(algo)) {
     DDP_TRY(check_common(p, n, dtype));
     DDP_TRY(check_divisor(divisor));
+    if (n == 0) return DDP_OK;  // a no-op whatever the pointers
     DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
     const int es = esize(dtype);
     std::vector<std::pair<uintptr_t, uintptr_t>> rg;
@@ -686,12 +703,14 @@ ddp_status ddp_allreduce(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtyp
 
 ddp_status ddp_allreduce_ex(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
                             ddp_algo algo, uint32_t flags, cudaStream_t stream) {
+  DDP_NVTX("ddp_allreduce_ex");
   DDP_TRY(check_common(p, n, dtype));
   DDP_TRY(check_divisor(divisor));
   DDP_TRY(check_algo(algo));
   DDP_CHECK((flags & ~static_cast<uint32_t>(DDP_FLAG_ROUND_EACH_HOP)) == 0, DDP_ERR_ARG, "unknown flags");
   const bool hop = (flags & DDP_FLAG_ROUND_EACH_HOP) != 0;
   DDP_CHECK(!hop || dtype == DDP_BFLOAT16, DDP_ERR_DTYPE, "DDP_FLAG_ROUND_EACH_HOP is a bf16 variant");
+  if (n == 0) return DDP_OK;  // a no-op whatever the pointers
   DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
   const int es = esize(dtype);
   std::vector<std::pair<uintptr_t, uintptr_t>> rg;
@@ -710,10 +729,12 @@ ddp_status ddp_allreduce_ex(void* const* bufs, int32_t p, int64_t n, ddp_dtype d
 
 ddp_status ddp_reduce_scatter(const void* const* in, void* const* out, int32_t p, int64_t n, ddp_dtype dtype,
                               float divisor, ddp_own own, ddp_algo algo, cudaStream_t stream) {
+  DDP_NVTX("ddp_reduce_scatter");
   DDP_TRY(check_common(p, n, dtype));
   DDP_TRY(check_divisor(divisor));
   DDP_TRY(check_algo(algo));
   DDP_TRY(check_own(own));
+  if (n == 0) return DDP_OK;  // a no-op whatever the pointers
   DDP_TRY(check_ptrs(in, p, "in"));
   DDP_TRY(check_ptrs(const_cast<const void* const*>(out), p, "out"));
   if (own == DDP_OWN_RANK)
@@ -743,9 +764,11 @@ ddp_status ddp_reduce_scatter(const void* const* in, void* const* out, int32_t p
 
 ddp_status ddp_allgather(const void* const* in, void* const* out, int32_t p, int64_t m, ddp_dtype dtype,
                          ddp_own own, ddp_algo algo, cudaStream_t stream) {
+  DDP_NVTX("ddp_allgather");
   DDP_TRY(check_common(p, m, dtype));
   DDP_TRY(check_algo(algo));
   DDP_TRY(check_own(own));
+  if (m == 0) return DDP_OK;  // a no-op whatever the pointers
   DDP_TRY(check_ptrs(in, p, "in"));
   DDP_TRY(check_ptrs(const_cast<const void* const*>(out), p, "out"));
   const int es = esize(dtype);
@@ -782,9 +805,11 @@ ddp_status ddp_allgather(const void* const* in, void* const* out, int32_t p, int
 
 ddp_status ddp_broadcast(void* const* bufs, int32_t p, int64_t nbytes, int32_t root, ddp_algo algo,
                          cudaStream_t stream) {
+  DDP_NVTX("ddp_broadcast");
   DDP_TRY(check_common(p, nbytes, DDP_FLOAT32));
   DDP_TRY(check_algo(algo));
   DDP_CHECK(root >= 0 && root < p, DDP_ERR_ARG, "root out of range");
+  if (nbytes == 0) return DDP_OK;  // a no-op whatever the pointers
   DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
   std::vector<std::pair<uintptr_t, uintptr_t>> rg;
   for (int r = 0; r < p; ++r) rg.push_back(range_of(bufs[r], nbytes));
@@ -812,6 +837,7 @@ ddp_status ddp_broadcast(void* const* bufs, int32_t p, int64_t nbytes, int32_t r
 ddp_status ddp_broadcast_coalesced(int32_t p, int32_t k, void* const* tensors, const int64_t* nbytes,
                                    int32_t root, int64_t bucket_cap_bytes, ddp_algo algo,
                                    cudaStream_t stream) {
+  DDP_NVTX("ddp_broadcast_coalesced");
   DDP_TRY(check_common(p, 0, DDP_FLOAT32));
   DDP_TRY(check_algo(algo));
   DDP_CHECK(k >= 0, DDP_ERR_ARG, "k must be >= 0");
@@ -928,6 +954,7 @@ ddp_status ddp_broadcast_coalesced(int32_t p, int32_t k, void* const* tensors, c
 
 ddp_status ddp_bucket_allreduce(int32_t p, int32_t k, void* const* grads, const int64_t* numel,
                                 const int64_t* offset, ddp_dtype dtype, float divisor, cudaStream_t stream) {
+  DDP_NVTX("ddp_bucket_allreduce");
   DDP_TRY(check_bucket_args(p, k, numel, offset, dtype));
   DDP_TRY(check_divisor(divisor));
   const int es = esize(dtype);
@@ -1176,6 +1203,7 @@ ddp_status ddp_reducer_bucket(const ddp_reducer* h, int32_t b, int64_t* numel, v
 
 ddp_status ddp_reducer_sync(ddp_reducer* h, float divisor, float predivide, ddp_algo algo, ddp_sync_mode mode,
                             cudaStream_t stream) {
+  DDP_NVTX("ddp_reducer_sync");
   DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
   DDP_TRY(check_divisor(divisor));
   DDP_TRY(check_divisor(predivide));
@@ -1241,6 +1269,7 @@ ddp_status ddp_reducer_prepare(ddp_reducer* h) {
 
 ddp_status ddp_reducer_mark_ready(ddp_reducer* h, int32_t tensor, float divisor, cudaEvent_t ready,
                                   cudaStream_t comm_stream, int32_t* fired) {
+  DDP_NVTX("ddp_reducer_mark_ready");
   DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
   DDP_CHECK(tensor >= 0 && tensor < h->k, DDP_ERR_ARG, "tensor index out of range");
   DDP_TRY(check_divisor(divisor));
@@ -1294,18 +1323,22 @@ ddp_status ddp_reducer_rebuild(ddp_reducer* h, const int32_t* order) {
 ddp_status ddp_allreduce_persistent(void* const* bufs, int32_t p, int64_t n, ddp_dtype dtype, float divisor,
                                     int64_t timeout_ns, int32_t fault_rank, int32_t fault_step, int32_t* status,
                                     cudaStream_t stream) {
+  DDP_NVTX("ddp_allreduce_persistent");
   DDP_TRY(check_common(p, n, dtype));
   DDP_TRY(check_divisor(divisor));
-  DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
   DDP_CHECK(timeout_ns >= 0, DDP_ERR_ARG, "timeout_ns must be >= 0");
   const int32_t T = 2 * (p - 1);
   DDP_CHECK(fault_rank == -1 || (fault_rank >= 0 && fault_rank < p && fault_step >= 0 && fault_step < T),
             DDP_ERR_ARG, "fault_rank must be -1 or a rank, fault_step a step in [0, 2(p-1))");
+  if (n == 0) {  // a no-op whatever the pointers; the status block still reads "no error"
+    if (status) DDP_CUDA(cudaMemsetAsync(status, 0, 4 * sizeof(int32_t), stream), "status reset");
+    return DDP_OK;
+  }
+  DDP_TRY(check_ptrs(const_cast<const void* const*>(bufs), p, "bufs"));
   std::vector<std::pair<uintptr_t, uintptr_t>> rg;
   for (int r = 0; r < p; ++r) rg.push_back(range_of(bufs[r], n * esize(dtype)));
   DDP_CHECK(disjoint(rg), DDP_ERR_ARG, "replica buffers overlap");
   if (status) DDP_CUDA(cudaMemsetAsync(status, 0, 4 * sizeof(int32_t), stream), "status reset");
-  if (n == 0) return DDP_OK;
   if (p == 1) return run_fused(const_cast<const void* const*>(bufs), bufs, 1, n, dtype, divisor, false, 0, false,
                                stream);
   const int max_blocks = ring_persistent_max_blocks();
@@ -1375,9 +1408,11 @@ ddp_status ddp_ring_create(ddp_ring** handle, ddp_op op, void* const* in, void* 
   *handle = nullptr;
   DDP_CHECK(op >= DDP_OP_ALLREDUCE && op <= DDP_OP_BROADCAST, DDP_ERR_ARG, "unknown op");
   DDP_TRY(check_common(p, n, op == DDP_OP_BROADCAST ? DDP_FLOAT32 : dtype));
-  DDP_TRY(check_ptrs(const_cast<const void* const*>(in), p, "in"));
+  DDP_CHECK(in != nullptr, DDP_ERR_ARG, "in array is null");
+  if (n > 0) DDP_TRY(check_ptrs(const_cast<const void* const*>(in), p, "in"));
   const bool needs_out = (op == DDP_OP_REDUCE_SCATTER || op == DDP_OP_ALLGATHER);
-  if (needs_out) DDP_TRY(check_ptrs(const_cast<const void* const*>(out), p, "out"));
+  DDP_CHECK(!needs_out || out != nullptr, DDP_ERR_ARG, "out array is null");
+  if (needs_out && n > 0) DDP_TRY(check_ptrs(const_cast<const void* const*>(out), p, "out"));
   if (op == DDP_OP_ALLREDUCE || op == DDP_OP_REDUCE_SCATTER) DDP_TRY(check_divisor(divisor));
   if (op != DDP_OP_BROADCAST) DDP_TRY(check_own(own));
   if (op == DDP_OP_BROADCAST) DDP_CHECK(root >= 0 && root < p, DDP_ERR_ARG, "root out of range");
@@ -1421,6 +1456,7 @@ int32_t ddp_ring_num_steps(const ddp_ring* h) { return h ? h->plan.nsteps : -1; 
 int32_t ddp_ring_steps_done(const ddp_ring* h) { return h ? h->plan.done : -1; }
 
 ddp_status ddp_ring_step(ddp_ring* h) {
+  DDP_NVTX("ddp_ring_step");
   DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
   return h->plan.step(h->stream);
 }

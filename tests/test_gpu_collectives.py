@@ -196,6 +196,29 @@ def test_fused_coalesced_broadcast_launch_split(k, launches):
     _no_device_error()
 
 
+def test_zero_sizes_accept_empty_tensors():
+    """Empty tensors have no storage (a null data pointer): a zero-size call
+    is a no-op whatever its pointers, for every entry point."""
+    p = 4
+    empty = [torch.empty(0, dtype=torch.float32, device="cuda") for _ in range(p)]
+    for algo in ALGOS + [D.DDP_ALGO_RECURSIVE_DOUBLING, D.DDP_ALGO_RABENSEIFNER, D.DDP_ALGO_TREE]:
+        D.ddp_allreduce(empty, 0, D.DDP_FLOAT32, 4.0, algo)
+    for algo in (D.DDP_ALGO_FUSED, D.DDP_ALGO_RING_STEPS):
+        for own in (D.DDP_OWN_RANK, D.DDP_OWN_RING):
+            D.ddp_reduce_scatter(empty, empty, 0, D.DDP_FLOAT32, 1.0, own, algo)
+        D.ddp_allgather(empty, empty, 0, D.DDP_FLOAT32, D.DDP_OWN_RANK, algo)
+        D.ddp_broadcast(empty, 0, 1, algo)
+    status = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+    D.ddp_allreduce_persistent(empty, 0, D.DDP_FLOAT32, 4.0, 0, -1, 0, status)
+    torch.cuda.synchronize()
+    assert status.cpu().tolist() == [0, 0, 0, 0]
+    # the scalar arguments are still checked
+    with pytest.raises(D.DDPError) as e:
+        D.ddp_allreduce(empty, 0, D.DDP_FLOAT32, 0.0)
+    assert e.value.status == D.DDP_ERR_ARG
+    _no_device_error()
+
+
 def test_zero_sizes_are_noops():
     devs, hosts, _ = make_replicas(4, 16, "f32")
     D.ddp_allreduce(devs, 0, D.DDP_FLOAT32, 4.0)

@@ -351,3 +351,45 @@ def test_llama_bf16_sync_and_buffer_broadcast_sampled_parity():
     torch.cuda.synchronize()
     _check_sync_sampled(cfg, red, grads, np.random.default_rng(6), per_bucket=300)
     assert D.ddp_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "resnet50"])
+def test_sync_reads_what_the_kernel_before_it_wrote(name):
+    """The whole-Reducer sync is launched as a programmatic dependent of the
+    kernel before it, and the coalesced broadcast lets its dependent start
+    early. Here that broadcast writes the gradients themselves (replica 0's
+    copied to every replica) and the sync follows on the same stream with no
+    host synchronisation: the sync must reduce the broadcast values, i.e. p
+    copies of replica 0's gradients summed in ring order and divided by D."""
+    cfg = W.CONFIGS[name]
+    p = cfg["p"]
+    grads, _ = W.make_grads(cfg)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    numel = W.numels(cfg)
+    starts = W.tensor_starts(cfg)
+    s = torch.cuda.current_stream()
+    nbytes = [t.numel() * t.element_size() for t in grads[0]]
+    for rep in range(3):
+        broadcast_buffers(grads, 0, 0, D.DDP_ALGO_FUSED, s)
+        red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE, 1.0, s)
+        if rep == 0:
+            torch.cuda.synchronize()
+            _, offset, bnumel = ob.bucket_layout(numel, red.buckets)
+            rng = np.random.default_rng(11)
+            for b, members in enumerate(red.buckets):
+                t = members[int(rng.integers(0, len(members)))]
+                idx = np.unique(np.concatenate([np.arange(min(64, numel[t])),
+                                                rng.integers(0, numel[t], size=min(512, numel[t]))]))
+                x0 = W.host_values(cfg, 0, starts[t] + idx)
+                # every replica holds replica 0's values: fold p copies in fp32, divide once
+                acc = x0.copy()
+                for _ in range(p - 1):
+                    acc = (acc + x0).astype(np.float32)
+                want = (acc / np.float32(W.divisor(cfg))).astype(np.float32)
+                for r in range(p):
+                    assert_bit_equal(to_host(grads[r][t])[idx], want, f"tensor {t} replica {r}")
+    torch.cuda.synchronize()
+    for t in range(len(numel)):
+        for r in range(1, p):
+            assert torch.equal(grads[r][t].view(torch.int32), grads[0][t].view(torch.int32))
+    assert D.ddp_device_error() == 0
