@@ -30,6 +30,17 @@
  *     once the scalar arguments are valid; the buffer pointers are then not
  *     read and may be NULL (an empty tensor has no storage). A ddp_ring
  *     handle of n == 0 (zero steps) still needs non-NULL pointer arrays.
+ *   - Call log: with the environment variable DDP_RING_LOG=<path> set when
+ *     the library first logs, each collective call (ddp_allreduce, _ex,
+ *     _persistent, ddp_reduce_scatter, ddp_allgather, ddp_broadcast,
+ *     _coalesced, ddp_bucket_allreduce, ddp_reducer_sync) appends one JSON
+ *     line to <path>: op, algo, p, n, dtype, bytes_algorithmic (inputs read
+ *     once, outputs written once), bytes_per_rank (what one simulated rank
+ *     sends in the method's schedule, the pages' per-rank byte counter),
+ *     status and elapsed_us (CUDA events around the call; null inside a stream
+ *     capture or on failure). A timed call waits for its own completion, so
+ *     with the log on, calls are synchronous. Without the variable nothing is
+ *     recorded and nothing waits.
  *   - Floating point: the sum of p contributions is accumulated in fp32 in
  *     ring order, by IEEE round-to-nearest additions (no FMA contraction, no
  *     reassociation); the scale is one IEEE division; bf16 results are
