@@ -19,6 +19,18 @@
 namespace ddp {
 namespace {
 
+// A replica's 16 bytes, with a hint that L2 fetch the surrounding 256-byte
+// block from DRAM. Measured on GB300 over the model-shaped syncs: 0.4 % faster
+// than a plain load; L1::no_allocate or an L2 evict-first policy instead cost
+// 3 %.
+__device__ __forceinline__ uint4 ld_prefetch256(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 struct View {
   void* const* ptr;
   const int64_t* start;
@@ -97,7 +109,7 @@ __device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divi
     if constexpr (P > 0) {
       uint4 w[P];
 #pragma unroll
-      for (int j = 0; j < P; ++j) w[j] = *reinterpret_cast<const uint4*>(base[j] + x);
+      for (int j = 0; j < P; ++j) w[j] = ld_prefetch256(base[j] + x);
       Vec<T>::unpack(w[0], acc);
 #pragma unroll
       for (int j = 1; j < P; ++j) {
