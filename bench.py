@@ -203,6 +203,25 @@ def cores_used() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU's model name, from lscpu (Arm hosts) or /proc/cpuinfo."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 def algo_code(name):
     import ring_all_reduce_ddp_gb300 as D
     return {"fused": D.DDP_ALGO_FUSED, "ldst": D.DDP_ALGO_FUSED_LDST, "tma": D.DDP_ALGO_FUSED_TMA,
@@ -458,7 +477,7 @@ def run_ours(args, ranks: Ranks):
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
         nbytes, secs, desc = oracle_sync_sample(cfg, args.cpu_budget_s)
         cpu = {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
-               "host_cores_available": cores_used()}
+               "host_cores_available": cores_used(), "cpu_model": cpu_model()}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ranks.world, "steps": args.steps,
@@ -541,7 +560,8 @@ def run_reference(args, ranks: Ranks):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg["dtype"],
         "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.config], "p": p, "algo": "oracle literal ring"},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle", "cores": 1, "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle", "cores": 1, "sample": desc,
+                         "host_cores_available": cores_used(), "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
