@@ -56,6 +56,12 @@
 extern "C" {
 #endif
 
+/* The library is built with hidden symbol visibility; the entry points
+ * declared in this header are the only symbols it exports. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
 #define DDP_MAX_P 256
 
 typedef enum {
@@ -430,6 +436,10 @@ int64_t ddp_kernel_launches(void);
 const char* ddp_last_error(void);
 /* Fixed name of a status code. */
 const char* ddp_status_string(ddp_status s);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
 
 #ifdef __cplusplus
 }

@@ -21,9 +21,11 @@ LIB = os.path.join(PKG, "libddp_ring.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No FMA contraction, IEEE division and square root, no flush-to-zero: the sums
-# must be the exact ring-order fp32 left folds.
+# must be the exact ring-order fp32 left folds. Hidden visibility: only the
+# entry points that include/ddp_ring.h declares are exported.
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-prec-div=true", "-ftz=false",
-              "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+              "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+              "-Xcompiler", "-fvisibility-inlines-hidden", "-I", INCLUDE, "-I", CSRC]
 
 
 def nvcc() -> str:
@@ -42,6 +44,7 @@ def _stale() -> bool:
         return True
     t = os.path.getmtime(LIB)
     deps = _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) \
+        + [os.path.join(CSRC, "exports.map")] \
         + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 
@@ -64,7 +67,8 @@ def build_library(force: bool = False, verbose_ptxas: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra), _sources()))
     tmp = LIB + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+    cmd = [nvcc(), *ARCH, "-shared", "-Xlinker", "--version-script=" + os.path.join(CSRC, "exports.map"), "-o", tmp,
+           *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -35,6 +35,9 @@ def test_every_declared_symbol_is_exported(L):
     out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (ddp_\w+)", out))
     assert declared <= exported, declared - exported
+    # and nothing else: no C++ internals or template instances leak out
+    every = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    assert every == exported == declared, sorted(every - declared)[:10]
     # and the binding knows every one of them, under the same name
     assert declared <= set(L.exported_symbols())
     for name in declared:
