@@ -85,7 +85,7 @@ typedef enum {
   DDP_ALGO_FUSED_LDST = 2,  /* one pass through registers (128-bit loads and stores) */
   DDP_ALGO_FUSED_TMA = 3,   /* one pass staged through shared memory by bulk
                                asynchronous copies (falls back to the register path
-                               when p > 64 or the replicas' alignments differ)      */
+                               when p > 16 or the replicas' alignments differ)      */
   /* Tree-shaped literal all-reduces ([DP] "Latency, trees, and choosing an
    * algorithm"; [COLL] tree all-reduce). ddp_allreduce only; the pairwise
    * tree order, not the ring's. bf16 buffers are widened into a stream-ordered
