@@ -14,13 +14,23 @@
  *     DEVICE pointers. They are read during the call and not kept, except by a
  *     ddp_ring handle, which keeps a copy until ddp_ring_destroy.
  *   - The caller owns every replica, input and output buffer. The library
- *     allocates only: a handle's workspace (freed by ddp_ring_destroy), and,
- *     for the literal ring schedule of a few one-shot calls, a stream-ordered
- *     temporary (cudaMallocAsync / cudaFreeAsync on the caller's stream).
+ *     allocates only:
+ *       a handle's device memory, freed by its destroy call: a ddp_ring's
+ *       workspace; a ddp_reducer's flat buckets, piece table and workspace;
+ *       stream-ordered temporaries (cudaMallocAsync / cudaFreeAsync on the
+ *       caller's stream) for the literal schedules of one-shot calls, the
+ *       persistent ring's step flags, and the fp32 workspace of the bf16
+ *       tree-shaped and persistent all-reduces.
+ *     ddp_reduce_scatter_noalloc allocates nothing.
  *   - Work is enqueued on the caller's stream and runs asynchronously to the
  *     host, as DDP's per-bucket futures do ([DDP] Part 2, "Step 3:
- *     finalize_backward"). No call synchronizes the device except
- *     ddp_ring_sync and ddp_device_error.
+ *     finalize_backward"). Only these wait for the device: ddp_ring_sync,
+ *     ddp_device_error, ddp_reducer_create (its piece-table upload),
+ *     ddp_reducer_rebuild (drains the device first), the destroy calls, and
+ *     every collective while the call log (DDP_RING_LOG) is on.
+ *   - Threads: calls on different handles, or handle-free calls, may run
+ *     from several host threads at once. One handle must not be used from
+ *     two threads at the same time.
  *   - Errors: every call returns a ddp_status. Argument errors are found on the
  *     host before anything is enqueued. A failed launch returns
  *     DDP_ERR_CUDA. ddp_last_error() gives this thread's last message.
