@@ -109,3 +109,22 @@ def test_bucket_assign_order_matches_oracle_rebuild(L, seed):
     assert got["buckets"] == rs.rebuild(numel, 4, first, cap, walk)
     with pytest.raises(L.DDPError):
         L.ddp_bucket_assign_order(numel, 4, first, cap, walk[:-1] + [walk[0]] if k > 1 else [5])
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """With the shared object absent the binding raises on first use: there is
+    no CPU or PyTorch fallback anywhere on the product path."""
+    import subprocess
+    import sys
+    code = (
+        "import ring_all_reduce_ddp_gb300 as D\n"
+        f"D.LIB_PATH = {str(tmp_path / 'absent.so')!r}\n"
+        "try:\n"
+        "    D.ddp_allreduce([0, 0], 0, D.DDP_FLOAT32, 2.0, stream=0)\n"
+        "except RuntimeError as e:\n"
+        "    assert 'not built' in str(e), e\n"
+        "    print('raised')\n"
+    )
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120,
+                       env=dict(os.environ, PYTHONPATH=ROOT))
+    assert r.returncode == 0 and r.stdout.strip() == "raised", r.stderr
