@@ -64,6 +64,33 @@ template <> struct Vec<__nv_bfloat16> {
   }
 };
 
+// ------------------------------------------ programmatic dependent launch
+// A kernel started by launch_pdl may begin while the kernel before it in the
+// stream drains. It calls pdl_wait() before its first memory access; that
+// returns once the earlier kernel has completed and its writes are visible
+// (at once for a kernel launched without the attribute). pdl_trigger() lets
+// the next such kernel start launching; it fires for a grid only once every
+// block has executed it, so a dependent never takes the place of a block of
+// the grid before it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ------------------------------------------------------------ argument blocks
 
 // Fused one-pass reduction (all-reduce, reduce-scatter).

@@ -56,7 +56,7 @@ __device__ __forceinline__ int find_piece(const int32_t* tile0, int n, int32_t b
 // which each block executes once, before its first data access.
 __device__ __forceinline__ void wait_previous_grid(bool& waited) {
   if (!waited) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     waited = true;
   }
 }
@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_cons
 // Piece table in device memory (every bucket of a Reducer in one launch).
 template <typename T, int P>
 __global__ void __launch_bounds__(kThreads) k_bucket_allreduce_table(const BucketTable t, float divisor) {
+  pdl_trigger();
   const View v{t.ptr, t.start, t.len, t.slot, t.origin, t.tile0, t.npieces, t.p};
   bucket_tiles<T, P>(v, divisor);
 }

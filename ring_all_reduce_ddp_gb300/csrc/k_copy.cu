@@ -79,6 +79,8 @@ __device__ __forceinline__ void copy_to_all(const char* s, char* const* d, int n
 
 // ---------------------------------------------------------------- kernels
 __global__ void __launch_bounds__(kThreads) k_pair_copy(const __grid_constant__ PairCopyArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int j = blockIdx.y;
   const int64_t nb = a.nbytes[j];
   const int64_t ntiles = (nb + kTileBytes - 1) / kTileBytes;
@@ -92,6 +94,8 @@ __global__ void __launch_bounds__(kThreads) k_pair_copy(const __grid_constant__ 
 
 template <int U>
 __global__ void __launch_bounds__(kThreads) k_fanout(const __grid_constant__ FanoutArgs a) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int64_t kTile = fan_tile_bytes<U>();
   const int j = blockIdx.y;
   const int64_t ntiles = (a.nbytes + kTile - 1) / kTile;
@@ -117,6 +121,8 @@ __device__ __forceinline__ int find_tile_owner(const int32_t* tile0, int nseg, i
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_seg_copy(const __grid_constant__ SegCopyArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int32_t b = blockIdx.x;
   const int s = find_tile_owner(a.tile0, a.nseg, b);
   const int64_t b0 = static_cast<int64_t>(b - a.tile0[s]) * kSegTileBytes;
@@ -154,6 +160,8 @@ __global__ void __launch_bounds__(kThreads) k_multi_fanout(const __grid_constant
 // bf16, 32 of fp32) when the bf16 side is 16-byte aligned and the fp32 side
 // 32-byte aligned; the rest element by element.
 __global__ void __launch_bounds__(kThreads) k_convert(const __grid_constant__ ConvertArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int j = blockIdx.y;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -202,39 +210,41 @@ cudaError_t launch_pair_copy(const PairCopyArgs& a, cudaStream_t s) {
   for (int j = 0; j < a.njobs; ++j) maxb = a.nbytes[j] > maxb ? a.nbytes[j] : maxb;
   if (maxb == 0) return cudaSuccess;
   const dim3 grid(grid_x_for((maxb + kTileBytes - 1) / kTileBytes, a.njobs), a.njobs);
-  k_pair_copy<<<grid, kThreads, 0, s>>>(a);
+  const cudaError_t e = launch_pdl(k_pair_copy, grid, dim3(kThreads), 0, s, a);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s) {
   if (a.njobs <= 0 || a.nbytes <= 0 || a.ndst <= 0) return cudaSuccess;
+  cudaError_t e;
   if (a.ndst <= kFanFewDst) {
     constexpr int64_t t = fan_tile_bytes<4>();
-    k_fanout<4><<<dim3(grid_x_for((a.nbytes + t - 1) / t, a.njobs), a.njobs), kThreads, 0, s>>>(a);
+    e = launch_pdl(k_fanout<4>, dim3(grid_x_for((a.nbytes + t - 1) / t, a.njobs), a.njobs), dim3(kThreads), 0, s, a);
   } else {
     constexpr int64_t t = fan_tile_bytes<2>();
-    k_fanout<2><<<dim3(grid_x_for((a.nbytes + t - 1) / t, a.njobs), a.njobs), kThreads, 0, s>>>(a);
+    e = launch_pdl(k_fanout<2>, dim3(grid_x_for((a.nbytes + t - 1) / t, a.njobs), a.njobs), dim3(kThreads), 0, s, a);
   }
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_seg_copy(const SegCopyArgs& a, ddp_dtype dt, cudaStream_t s) {
   const int32_t ntiles = a.tile0[a.nseg];
   if (a.nseg <= 0 || ntiles <= 0) return cudaSuccess;
-  if (dt == DDP_BFLOAT16) k_seg_copy<__nv_bfloat16><<<ntiles, kThreads, 0, s>>>(a);
-  else k_seg_copy<float><<<ntiles, kThreads, 0, s>>>(a);
+  const cudaError_t e = dt == DDP_BFLOAT16
+                            ? launch_pdl(k_seg_copy<__nv_bfloat16>, dim3(ntiles), dim3(kThreads), 0, s, a)
+                            : launch_pdl(k_seg_copy<float>, dim3(ntiles), dim3(kThreads), 0, s, a);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t s) {
   if (a.njobs <= 0 || a.n <= 0) return cudaSuccess;
   const dim3 grid(grid_x_for((a.n + 8 * kThreads - 1) / (8 * kThreads), a.njobs), a.njobs);
-  k_convert<<<grid, kThreads, 0, s>>>(a);
+  const cudaError_t e = launch_pdl(k_convert, grid, dim3(kThreads), 0, s, a);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_multi_fanout(const MultiFanoutArgs& a, cudaStream_t s) {

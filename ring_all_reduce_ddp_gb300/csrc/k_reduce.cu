@@ -27,6 +27,8 @@ __device__ int g_device_error = 0;
 // ------------------------------------------------ fused, register-only path
 template <typename T, int P, bool HOP = false>
 __global__ void __launch_bounds__(kThreads) k_fused_reduce_ldst(const __grid_constant__ FusedArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int p = (P > 0) ? P : a.p;
   const int c = blockIdx.y;
   const int64_t lo = static_cast<int64_t>(c) * a.cs;
@@ -321,6 +323,8 @@ __device__ __forceinline__ int sent_chunk(int r, int step, int shift, int p) {
 // fp32 all-reduce, partials in the replicas themselves: rank r+1's copy of
 // chunk (r - s) mod p becomes local + received; the last step also divides.
 __global__ void __launch_bounds__(kThreads) k_rs_step_inplace_f32(const __grid_constant__ RingStepArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int p = a.p;
   const int r = blockIdx.y;
   const int d = (r + 1) % p;
@@ -383,6 +387,8 @@ __global__ void __launch_bounds__(kThreads) k_rs_step_inplace_f32(const __grid_c
 // round(fl32(sum / divisor)) to its output.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_rs_step_ws(const __grid_constant__ RingStepArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int p = a.p;
   const int r = blockIdx.y;
   const int d = (r + 1) % p;
@@ -568,15 +574,16 @@ template <typename T, bool HOP>
 cudaError_t fused_ldst(const FusedArgs& a, cudaStream_t s) {
   constexpr int V = Vec<T>::N;
   const dim3 grid(blocks_per_chunk(a.cs / V + 1, kThreads, a.p), a.p);
+  cudaError_t e;
   switch (a.p) {
-    case 2: k_fused_reduce_ldst<T, 2, HOP><<<grid, kThreads, 0, s>>>(a); break;
-    case 4: k_fused_reduce_ldst<T, 4, HOP><<<grid, kThreads, 0, s>>>(a); break;
-    case 8: k_fused_reduce_ldst<T, 8, HOP><<<grid, kThreads, 0, s>>>(a); break;
-    case 16: k_fused_reduce_ldst<T, 16, HOP><<<grid, kThreads, 0, s>>>(a); break;
-    default: k_fused_reduce_ldst<T, 0, HOP><<<grid, kThreads, 0, s>>>(a); break;
+    case 2: e = launch_pdl(k_fused_reduce_ldst<T, 2, HOP>, grid, dim3(kThreads), 0, s, a); break;
+    case 4: e = launch_pdl(k_fused_reduce_ldst<T, 4, HOP>, grid, dim3(kThreads), 0, s, a); break;
+    case 8: e = launch_pdl(k_fused_reduce_ldst<T, 8, HOP>, grid, dim3(kThreads), 0, s, a); break;
+    case 16: e = launch_pdl(k_fused_reduce_ldst<T, 16, HOP>, grid, dim3(kThreads), 0, s, a); break;
+    default: e = launch_pdl(k_fused_reduce_ldst<T, 0, HOP>, grid, dim3(kThreads), 0, s, a); break;
   }
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 }  // namespace
 
@@ -683,17 +690,17 @@ cudaError_t launch_fused_reduce(const FusedArgs& a, ddp_dtype dt, bool staged, c
 
 cudaError_t launch_rs_step_inplace_f32(const RingStepArgs& a, cudaStream_t s) {
   const dim3 grid(blocks_per_chunk(a.cs / 4 + 1, kThreads * kU, a.p), a.p);
-  k_rs_step_inplace_f32<<<grid, kThreads, 0, s>>>(a);
+  const cudaError_t e = launch_pdl(k_rs_step_inplace_f32, grid, dim3(kThreads), 0, s, a);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_rs_step_ws(const RingStepArgs& a, ddp_dtype dt, cudaStream_t s) {
   const dim3 grid(blocks_per_chunk(a.cs, kThreads * kU, a.p), a.p);
-  if (dt == DDP_FLOAT32) k_rs_step_ws<float><<<grid, kThreads, 0, s>>>(a);
-  else k_rs_step_ws<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a);
+  const cudaError_t e = dt == DDP_FLOAT32 ? launch_pdl(k_rs_step_ws<float>, grid, dim3(kThreads), 0, s, a)
+                                          : launch_pdl(k_rs_step_ws<__nv_bfloat16>, grid, dim3(kThreads), 0, s, a);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int ring_persistent_max_blocks() {

@@ -13,6 +13,8 @@ namespace {
 constexpr int kAddU = 4;  // float4 vectors in flight per thread
 
 __global__ void __launch_bounds__(kThreads) k_pair_add(const __grid_constant__ PairAddArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int j = blockIdx.y;
   const int64_t lo = a.lo[j], hi = a.hi[j];
   if (hi <= lo) return;
@@ -86,9 +88,9 @@ cudaError_t launch_pair_add(const PairAddArgs& a, cudaStream_t s) {
   const int64_t need = (maxlen / 4 + kThreads * kAddU - 1) / (kThreads * kAddU);
   if (bx > need) bx = need;
   if (bx < 1) bx = 1;
-  k_pair_add<<<dim3(static_cast<unsigned>(bx), a.njobs), kThreads, 0, s>>>(a);
+  const cudaError_t e = launch_pdl(k_pair_add, dim3(static_cast<unsigned>(bx), a.njobs), dim3(kThreads), 0, s, a);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace ddp
