@@ -63,3 +63,35 @@ def test_in_place_bucket_past_2_to_the_31_elements(big):
     D.ddp_bucket_allreduce([[b] for b in big], [N], [0], D.DDP_FLOAT32, 2.0)
     torch.cuda.synchronize()
     _check(big, 2.0)
+
+
+@pytest.fixture(scope="module")
+def big_bf16():
+    free, _ = torch.cuda.mem_get_info()
+    if free < 3 * P * N * 2:
+        pytest.skip("not enough device memory for the > 2^31-element bf16 case")
+    return [torch.empty(N, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+
+
+def _check_bf16(bufs, divisor):
+    idx = _sample()
+    ins = [synth.values_np("uniform", 4343, r, idx, 1.0, "bf16") for r in range(P)]
+    want, _ = orc.allreduce(ins, N, divisor, "bf16", idx=idx)
+    t_idx = torch.from_numpy(idx).cuda()
+    for r in range(P):
+        assert_bit_equal(to_host(bufs[r][t_idx]), want[r], f"replica {r}")
+
+
+@pytest.mark.parametrize("path", ["fused", "in_place_bucket"])
+def test_bf16_past_2_to_the_31_elements(big_bf16, path):
+    """bf16 replicas of 2^31 + 1027 elements: the flat fused kernel and the
+    in-place bucket kernel (64 KB tiles) on sampled elements."""
+    for r, b in enumerate(big_bf16):
+        synth.fill_(b, "uniform", 4343, r)
+    if path == "fused":
+        D.ddp_allreduce(big_bf16, N, D.DDP_BFLOAT16, 2.0, D.DDP_ALGO_FUSED)
+    else:
+        D.ddp_bucket_allreduce([[b] for b in big_bf16], [N], [0], D.DDP_BFLOAT16, 2.0)
+    torch.cuda.synchronize()
+    _check_bf16(big_bf16, 2.0)
+    assert D.ddp_device_error() == 0
