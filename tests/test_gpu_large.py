@@ -1,6 +1,6 @@
 """Maximum sizes: one replica buffer of more than 2^31 elements (8.6 GB of fp32
-per replica), so every 32-bit index would overflow. The fused, in-place and
-literal paths are checked on sampled elements (both sides of the chunk
+or 4.3 GB of bf16 per replica), so every 32-bit index would overflow. The
+fused, in-place and literal paths are checked on sampled elements (both sides of the chunk
 boundary, the ends, and random indices) against the oracle's ring restricted to
 those elements, from inputs regenerated on the host."""
 import numpy as np
