@@ -744,7 +744,12 @@ def run_overlap(args, ranks: Ranks):
     w = torch.randn(kdim, wmax, device="cuda", dtype=torch.bfloat16)
     y = torch.empty(n_tok, wmax, device="cuda", dtype=torch.bfloat16)
     compute = torch.cuda.current_stream()
-    comm = torch.cuda.Stream()
+    # the communication stream at normal priority, or at the device's highest
+    # (the block scheduler then starts pending all-reduce blocks ahead of the
+    # backward's GEMM blocks)
+    lo_prio, hi_prio = torch.cuda.Stream.priority_range()
+    comm_streams = {"normal": torch.cuda.Stream(priority=lo_prio), "high": torch.cuda.Stream(priority=hi_prio)}
+    comm = comm_streams["normal"]
 
     ready_events = [torch.cuda.Event() for _ in range(k)]
 
@@ -766,7 +771,8 @@ def run_overlap(args, ranks: Ranks):
         a.record(compute)
         for _ in range(reps):
             fn()
-        compute.wait_stream(comm)
+        for cs in comm_streams.values():
+            compute.wait_stream(cs)
         b.record(compute)
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
@@ -775,7 +781,9 @@ def run_overlap(args, ranks: Ranks):
     t_bwd = timed(lambda: backward(None), reps)
     flops = 4.0 * sum(n for n in numel if n >= 4096) * n_tok
     caps = [int(float(c) * (1 << 20)) for c in os.environ.get("OVERLAP_CAPS_MB", "0.25,1,5,25,100,100000").split(",")]
-    for cap in caps:
+    prios = os.environ.get("OVERLAP_PRIORITIES", "normal,high").split(",")
+    for cap, prio in [(c, q) for c in caps for q in prios]:
+        comm = comm_streams[prio]
         red = Reducer(grads, min(cfg["first_cap"], cap), cap)
 
         def overlapped():
@@ -790,6 +798,7 @@ def run_overlap(args, ranks: Ranks):
         t_se = timed(serial, reps)
         t_comm = timed(lambda: red.sync_gradients(divisor, D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE, 1.0, compute), reps)
         print(json.dumps({"overlap": args.config, "p": cfg["p"], "bucket_cap_mb": cap / (1 << 20),
+                          "comm_stream_priority": prio,
                           "buckets": len(red.buckets), "n_tok": n_tok,
                           "backward_ms": round(t_bwd, 4), "backward_tflops": round(flops / (t_bwd / 1e3) / 1e12, 1),
                           "sync_alone_ms": round(t_comm, 4), "overlapped_ms": round(t_ov, 4),
