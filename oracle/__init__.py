@@ -18,6 +18,9 @@ Modules
   bf16      bf16 <-> fp32 conversions from their definitions
   costs     the cost-model closed forms
   linear_dp data-parallel gradient averaging on a linear model
+  trees     recursive doubling, Rabenseifner and binomial-tree all-reduces
+  reducer_sim  bucket readiness (mark_variable_ready / mark_bucket_ready),
+            overlap timelines, and rebuilding buckets from a ready order
 
 Parity unpinned: none. Every function is pinned by a CPU test against values
 the pages print, closed forms, brute force or an independent library routine.
