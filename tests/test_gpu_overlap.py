@@ -145,3 +145,44 @@ def test_step_captured_in_a_cuda_graph_replays_bit_exactly(name):
         for r in range(p):
             for j in range(len(bufs_e[r])):
                 assert torch.equal(bufs_g[r][j], bufs_e[r][j])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_collectives_capture_into_cuda_graphs(dtype):
+    """Every collective form captures into a CUDA graph (including the
+    stream-ordered workspaces of the literal and bf16 paths, which become graph
+    memory nodes) and a replay gives the bits of the same call run eagerly."""
+    from tests.helpers import make_replicas
+    p, n = 8, 100003
+    tdt = D.DDP_FLOAT32 if dtype == "f32" else D.DDP_BFLOAT16
+    cases = [("allreduce", a) for a in (D.DDP_ALGO_FUSED, D.DDP_ALGO_FUSED_TMA, D.DDP_ALGO_RING_STEPS,
+                                        D.DDP_ALGO_RECURSIVE_DOUBLING, D.DDP_ALGO_RABENSEIFNER, D.DDP_ALGO_TREE)]
+    cases += [("reduce_scatter", a) for a in (D.DDP_ALGO_FUSED, D.DDP_ALGO_RING_STEPS)]
+    cases += [("allgather", a) for a in (D.DDP_ALGO_FUSED, D.DDP_ALGO_RING_STEPS)]
+    view = torch.int32 if dtype == "f32" else torch.int16
+    for op, algo in cases:
+        eager, _, _ = make_replicas(p, n, dtype, "normal", seed=77)
+        graphed, _, _ = make_replicas(p, n, dtype, "normal", seed=77)
+        m = -(-n // p)
+        outs_e = [torch.zeros(p * m, dtype=eager[0].dtype, device="cuda") for _ in range(p)]
+        outs_g = [torch.zeros(p * m, dtype=eager[0].dtype, device="cuda") for _ in range(p)]
+
+        def call(bufs, outs, stream=None):
+            if op == "allreduce":
+                D.ddp_allreduce(bufs, n, tdt, float(p), algo, stream)
+            elif op == "reduce_scatter":
+                D.ddp_reduce_scatter(bufs, outs, n, tdt, float(p), D.DDP_OWN_RING, algo, stream)
+            else:
+                D.ddp_allgather([b[:m] for b in bufs], outs, m, tdt, D.DDP_OWN_RANK, algo, stream)
+
+        call(eager, outs_e)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call(graphed, outs_g)
+        g.replay()
+        torch.cuda.synchronize()
+        for r in range(p):
+            assert torch.equal(graphed[r].view(view), eager[r].view(view)), (op, algo, r)
+            assert torch.equal(outs_g[r].view(view), outs_e[r].view(view)), (op, algo, r)
+        del g
+    assert D.ddp_device_error() == 0
