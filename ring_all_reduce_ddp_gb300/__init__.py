@@ -123,10 +123,17 @@ def _check(rc: int):
 
 
 def _ptr(x) -> int:
+    """A device address: an int is passed through (the caller vouches for it);
+    a tensor must be a contiguous device tensor, since the library sees only
+    its first byte and its element count."""
     if x is None:
         return 0
     if isinstance(x, int):
         return x
+    if not x.is_cuda:
+        raise ValueError("tensors passed to the library must live on a CUDA device")
+    if not x.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
     return int(x.data_ptr())
 
 
@@ -311,6 +318,11 @@ class DDPReducer:
         self.k = len(grads[0])
         self.dtype = _dtype(grads[0][0].dtype)
         numel = [g.numel() for g in grads[0]]
+        for r, row in enumerate(grads):  # one dtype and one shape list for every replica
+            if len(row) != self.k or [g.numel() for g in row] != numel:
+                raise ValueError(f"replica {r} does not have replica 0's tensor sizes")
+            if any(g.dtype != grads[0][0].dtype for g in row):
+                raise ValueError("all gradient tensors of a Reducer must share one dtype")
         h = ctypes.c_void_p(0)
         self._grads = _ptrs([g for row in grads for g in row])
         _check(lib().ddp_reducer_create(ctypes.byref(h), self.p, self.k, self._grads, _i64s(numel), self.dtype,

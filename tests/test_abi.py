@@ -128,3 +128,27 @@ def test_missing_library_fails_loudly(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120,
                        env=dict(os.environ, PYTHONPATH=ROOT))
     assert r.returncode == 0 and r.stdout.strip() == "raised", r.stderr
+
+
+def test_binding_rejects_tensors_it_cannot_pass_as_pointers(L):
+    """The library sees a first byte and an element count: the binding refuses
+    host tensors, non-contiguous views, and a Reducer whose replicas disagree
+    on sizes or mix dtypes, before anything reaches the library."""
+    torch = pytest.importorskip("torch")
+    host = [torch.zeros(8) for _ in range(2)]
+    with pytest.raises(ValueError, match="CUDA device"):
+        L.ddp_allreduce(host, 8, L.DDP_FLOAT32, 2.0, stream=0)
+    mixed = [[torch.zeros(4), torch.zeros(4, dtype=torch.bfloat16)] for _ in range(2)]
+    with pytest.raises(ValueError, match="one dtype"):
+        L.DDPReducer(mixed)
+    ragged = [[torch.zeros(4)], [torch.zeros(5)]]
+    with pytest.raises(ValueError, match="sizes"):
+        L.DDPReducer(ragged)
+
+
+@pytest.mark.gpu
+def test_binding_rejects_non_contiguous_views(L):
+    torch = pytest.importorskip("torch")
+    bufs = [torch.zeros(16, device="cuda")[::2] for _ in range(2)]
+    with pytest.raises(ValueError, match="contiguous"):
+        L.ddp_allreduce(bufs, 8, L.DDP_FLOAT32, 2.0)
