@@ -152,3 +152,15 @@ def test_binding_rejects_non_contiguous_views(L):
     bufs = [torch.zeros(16, device="cuda")[::2] for _ in range(2)]
     with pytest.raises(ValueError, match="contiguous"):
         L.ddp_allreduce(bufs, 8, L.DDP_FLOAT32, 2.0)
+
+
+def test_c_program_compiles_against_the_header_alone(L, tmp_path):
+    """The header is enough to build a C++ user of the library (no torch, no
+    Python): tests/c/abi_smoke.cpp compiles and links here; the GPU tests run it."""
+    from ring_all_reduce_ddp_gb300 import build as B
+    lib = B.build_library()
+    cmd = [B.nvcc(), *B.ARCH, "-O2", "-std=c++17", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c", "abi_smoke.cpp"), "-L", os.path.dirname(lib), "-lddp_ring",
+           "-o", str(tmp_path / "abi_smoke")]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
