@@ -33,7 +33,10 @@
  *     two threads at the same time.
  *   - Errors: every call returns a ddp_status. Argument errors are found on the
  *     host before anything is enqueued. A failed launch returns
- *     DDP_ERR_CUDA. ddp_last_error() gives this thread's last message.
+ *     DDP_ERR_CUDA. A stream-ordered temporary that cannot be allocated
+ *     returns DDP_ERR_NOMEM before any kernel of the call is enqueued, and
+ *     leaves no CUDA error pending. ddp_last_error() gives this thread's
+ *     last message.
  *   - Replica buffers of one call must be distinct and must not overlap.
  *     Alignment is not required; misaligned heads and tails take a scalar path.
  *   - 1 <= p <= DDP_MAX_P. n == 0 (or nbytes == 0) is a no-op returning DDP_OK
@@ -360,7 +363,11 @@ ddp_status ddp_reducer_destroy(ddp_reducer* handle);
  * ddp_reducer_rebuild rebuilds the buckets along `order` (a permutation of
  *   0..k-1, first-ready first) or, if order is NULL, along the observed order
  *   (DDP_ERR_STATE unless every tensor was marked); reallocates the flat
- *   buckets and tables (it synchronizes the device) and resets readiness. */
+ *   buckets and tables (it synchronizes the device) and resets readiness.
+ *   If the rebuild fails after the old buckets were released (an allocation
+ *   returns DDP_ERR_NOMEM), the handle keeps no buckets and no device memory:
+ *   ddp_reducer_sync, _prepare and _mark_ready then return DDP_ERR_STATE
+ *   until a rebuild succeeds; destroy works as always. */
 ddp_status ddp_reducer_prepare(ddp_reducer* handle);
 ddp_status ddp_reducer_mark_ready(ddp_reducer* handle, int32_t tensor, float divisor, cudaEvent_t ready,
                                   cudaStream_t comm_stream, int32_t* fired);

@@ -47,11 +47,7 @@ ddp_status allreduce_impl(void* const* bufs, int32_t p, int64_t n, ddp_dtype dty
     // replica's finished fp32 value is rounded to bf16 once at the end.
     const int64_t slot = (n * 4 + 255) / 256 * 256;
     void* wsv = nullptr;
-    const cudaError_t ea = cudaMallocAsync(&wsv, slot * p, stream);
-    if (ea != cudaSuccess) {
-      (void)cudaGetLastError();  // an allocation failure is not sticky: do not let a later launch report it
-      return fail(DDP_ERR_NOMEM, std::string("tree workspace: ") + cudaGetErrorString(ea));
-    }
+    DDP_TRY(alloc_async(&wsv, slot * p, stream, "tree workspace"));
     char* ws = static_cast<char*>(wsv);
     for (int r = 0; r < p; ++r) B[r] = reinterpret_cast<float*>(ws + slot * r);
     ConvertArgs cv;
@@ -289,7 +285,7 @@ ddp_status broadcast_coalesced_impl(int32_t p, int32_t k, void* const* tensors, 
   if (gmax == 0) return DDP_OK;
   const int64_t slot = (gmax + 255) / 256 * 256;
   void* wsv = nullptr;
-  DDP_CUDA(cudaMallocAsync(&wsv, slot * p, stream), "broadcast workspace allocation");
+  DDP_TRY(alloc_async(&wsv, slot * p, stream, "broadcast workspace allocation"));
   char* ws = static_cast<char*>(wsv);
   ddp_status rc = DDP_OK;
   for (size_t g = 0; g < groups.size() && rc == DDP_OK; ++g) {
@@ -379,11 +375,7 @@ ddp_status allreduce_persistent_impl(void* const* bufs, int32_t p, int64_t n, dd
     // run the fp32 ring there, round each finished value to bf16 once.
     const int64_t slot = (n * 4 + 255) / 256 * 256;
     void* wsv = nullptr;
-    const cudaError_t ea = cudaMallocAsync(&wsv, slot * p, stream);
-    if (ea != cudaSuccess) {
-      (void)cudaGetLastError();  // an allocation failure is not sticky: do not let a later launch report it
-      return fail(DDP_ERR_NOMEM, std::string("persistent ring workspace: ") + cudaGetErrorString(ea));
-    }
+    DDP_TRY(alloc_async(&wsv, slot * p, stream, "persistent ring workspace"));
     std::vector<void*> W(p);
     ConvertArgs cv;
     std::memset(&cv, 0, sizeof(cv));
@@ -422,7 +414,7 @@ ddp_status allreduce_persistent_impl(void* const* bufs, int32_t p, int64_t n, dd
   a.timeout_ns = timeout_ns > 0 ? timeout_ns : 1000000000LL;
   a.status = status;
   void* flags = nullptr;
-  DDP_CUDA(cudaMallocAsync(&flags, static_cast<size_t>(p) * B * kFlagStride * sizeof(int), stream), "step flags allocation");
+  DDP_TRY(alloc_async(&flags, static_cast<size_t>(p) * B * kFlagStride * sizeof(int), stream, "step flags allocation"));
   a.flags = static_cast<int*>(flags);
   cudaError_t e = cudaMemsetAsync(flags, 0, static_cast<size_t>(p) * B * kFlagStride * sizeof(int), stream);
   if (e == cudaSuccess) e = launch_ring_persistent(a, stream);
@@ -557,11 +549,10 @@ ddp_status ddp_ring_create(ddp_ring** handle, ddp_op op, void* const* in, void* 
   h->stream = stream;
   if (pl.needs_ws() && n > 0) {
     void* w = nullptr;
-    const cudaError_t e = cudaMalloc(&w, pl.ws_elems() * sizeof(float));
-    if (e != cudaSuccess) {
+    const ddp_status st = alloc_device(&w, pl.ws_elems() * sizeof(float), "handle workspace allocation");
+    if (st != DDP_OK) {
       delete h;
-      t_error = std::string("handle workspace allocation: ") + cudaGetErrorString(e);
-      return DDP_ERR_NOMEM;
+      return st;
     }
     pl.ws = static_cast<float*>(w);
   }

@@ -15,6 +15,24 @@ ddp_status fail(ddp_status s, const std::string& msg) {
   return s;
 }
 
+ddp_status alloc_async(void** ptr, size_t bytes, cudaStream_t s, const char* what) {
+  *ptr = nullptr;
+  const cudaError_t e = cudaMallocAsync(ptr, bytes, s);
+  if (e == cudaSuccess) return DDP_OK;
+  (void)cudaGetLastError();
+  *ptr = nullptr;
+  return fail(DDP_ERR_NOMEM, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+ddp_status alloc_device(void** ptr, size_t bytes, const char* what) {
+  *ptr = nullptr;
+  const cudaError_t e = cudaMalloc(ptr, bytes);
+  if (e == cudaSuccess) return DDP_OK;
+  (void)cudaGetLastError();
+  *ptr = nullptr;
+  return fail(DDP_ERR_NOMEM, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
 ddp_status cuda_fail(cudaError_t e, const char* where) {
   t_error = std::string(where) + ": " + cudaGetErrorString(e);
   return DDP_ERR_CUDA;
@@ -96,7 +114,7 @@ ddp_status run_plan_once(Plan& pl, cudaStream_t s) {
   pl.init();
   if (pl.needs_ws()) {
     void* w = nullptr;
-    DDP_CUDA(cudaMallocAsync(&w, pl.ws_elems() * sizeof(float), s), "workspace allocation");
+    DDP_TRY(alloc_async(&w, pl.ws_elems() * sizeof(float), s, "workspace allocation"));
     pl.ws = static_cast<float*>(w);
   }
   const ddp_status rc = pl.run_all(s);

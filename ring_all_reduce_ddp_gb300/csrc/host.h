@@ -50,6 +50,13 @@ struct NvtxRange {
 
 struct Plan;
 
+// A stream-ordered temporary (cudaMallocAsync on s). A failure returns
+// DDP_ERR_NOMEM with `what` in the error text, and clears CUDA's last error:
+// an allocation failure is not sticky and must not surface at a later launch.
+ddp_status alloc_async(void** ptr, size_t bytes, cudaStream_t s, const char* what);
+// The same for a handle's long-lived memory (cudaMalloc).
+ddp_status alloc_device(void** ptr, size_t bytes, const char* what);
+
 ddp_status fail(ddp_status s, const std::string& msg);
 ddp_status cuda_fail(cudaError_t e, const char* where);
 int esize(ddp_dtype dt);

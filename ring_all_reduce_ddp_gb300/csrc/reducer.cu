@@ -41,6 +41,9 @@ struct ddp_reducer {
   std::vector<char> marked;
   std::vector<int32_t> observed;  // ready order seen since the last prepare
   int32_t next_bucket = 0;
+  // A rebuild that failed part way leaves no buckets; until a later rebuild
+  // succeeds, sync and readiness calls refuse to run rather than do nothing.
+  bool unbuilt = false;
 };
 
 namespace {
@@ -108,8 +111,7 @@ ddp_status build_reducer_table(ddp_reducer* h) {
   std::memcpy(host.data() + o_origin, origin.data(), np * 4);
   std::memcpy(host.data() + o_tile0, tile0.data(), (np + 1) * 4);
   void* mem = nullptr;
-  cudaError_t e = cudaMalloc(&mem, total);
-  if (e != cudaSuccess) return fail(DDP_ERR_NOMEM, std::string("reducer piece table: ") + cudaGetErrorString(e));
+  DDP_TRY(alloc_device(&mem, total, "reducer piece table"));
   h->table_mem = mem;
   DDP_CUDA(cudaMemcpy(mem, host.data(), total, cudaMemcpyHostToDevice), "reducer piece table upload");
   unsigned char* d = static_cast<unsigned char*>(mem);
@@ -147,14 +149,12 @@ ddp_status reducer_build(ddp_reducer* h, const std::vector<int32_t>& walk, bool 
   }
   for (int32_t r = 0; r < p; ++r) {
     void* a = nullptr;
-    const cudaError_t e = cudaMalloc(&a, std::max<int64_t>(arena, 256));
-    if (e != cudaSuccess) return fail(DDP_ERR_NOMEM, std::string("reducer buckets: ") + cudaGetErrorString(e));
+    DDP_TRY(alloc_device(&a, std::max<int64_t>(arena, 256), "reducer buckets"));
     h->arenas.push_back(a);
   }
   if (h->dt == DDP_BFLOAT16 && p > 1 && h->ws_elems > 0) {
     void* w = nullptr;
-    const cudaError_t e = cudaMalloc(&w, h->ws_elems * sizeof(float));
-    if (e != cudaSuccess) return fail(DDP_ERR_NOMEM, std::string("reducer workspace: ") + cudaGetErrorString(e));
+    DDP_TRY(alloc_device(&w, h->ws_elems * sizeof(float), "reducer workspace"));
     h->ws = static_cast<float*>(w);
   }
   for (size_t b = 0; b < lists.size(); ++b) {
@@ -198,6 +198,7 @@ ddp_status reducer_sync_impl(ddp_reducer* h, float divisor, float predivide, ddp
   DDP_TRY(check_divisor(predivide));
   DDP_TRY(check_algo(algo));
   DDP_CHECK(mode == DDP_SYNC_FLATTEN || mode == DDP_SYNC_IN_PLACE, DDP_ERR_ARG, "unknown sync mode");
+  DDP_CHECK(!h->unbuilt, DDP_ERR_STATE, "the reducer's last rebuild failed; rebuild it again or destroy it");
   const int p = h->p;
   if (mode == DDP_SYNC_IN_PLACE) {
     DDP_CHECK(algo != DDP_ALGO_RING_STEPS, DDP_ERR_ARG, "the in-place sync is the fused form only");
@@ -314,6 +315,7 @@ ddp_status ddp_reducer_destroy(ddp_reducer* h) {
 
 ddp_status ddp_reducer_prepare(ddp_reducer* h) {
   DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
+  DDP_CHECK(!h->unbuilt, DDP_ERR_STATE, "the reducer's last rebuild failed; rebuild it again or destroy it");
   for (size_t b = 0; b < h->buckets.size(); ++b) h->pending[b] = static_cast<int32_t>(h->buckets[b].members.size());
   std::fill(h->marked.begin(), h->marked.end(), 0);
   h->observed.clear();
@@ -326,6 +328,7 @@ ddp_status ddp_reducer_mark_ready(ddp_reducer* h, int32_t tensor, float divisor,
   DDP_NVTX("ddp_reducer_mark_ready");
   DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
   DDP_CHECK(tensor >= 0 && tensor < h->k, DDP_ERR_ARG, "tensor index out of range");
+  DDP_CHECK(!h->unbuilt, DDP_ERR_STATE, "the reducer's last rebuild failed; rebuild it again or destroy it");
   DDP_TRY(check_divisor(divisor));
   DDP_CHECK(!h->marked[tensor], DDP_ERR_STATE,
             "tensor " + std::to_string(tensor) + " was already marked ready since the last ddp_reducer_prepare");
@@ -371,7 +374,16 @@ ddp_status ddp_reducer_rebuild(ddp_reducer* h, const int32_t* order) {
     seen[t] = 1;
   }
   DDP_CUDA(cudaDeviceSynchronize(), "synchronize before rebuilding buckets");
-  return reducer_build(h, walk, false);
+  const ddp_status st = reducer_build(h, walk, false);
+  if (st != DDP_OK) {  // release what the failed build allocated; keep the handle, bucket-less
+    const std::string msg = t_error;
+    reducer_free_device(h);
+    h->buckets.clear();
+    h->unbuilt = true;
+    return fail(st, msg + " (the reducer has no buckets until a rebuild succeeds)");
+  }
+  h->unbuilt = false;
+  return DDP_OK;
 }
 
 }  // extern "C"
