@@ -25,13 +25,13 @@ namespace ddp {
 __device__ int g_device_error = 0;
 
 // ------------------------------------------------ fused, register-only path
-// Vectors per thread: with p = 2 or 4 a vector needs only two or four loads, so
-// each thread takes four or two vectors and keeps eight 16-byte loads in
-// flight; larger p already does.
+// Vectors per thread (U): with p = 2 or 4 a vector needs only two or four
+// loads, so on large chunks each thread takes four or two vectors and keeps
+// eight 16-byte loads in flight; larger p already does.
 template <int P>
 __host__ __device__ constexpr int ldst_unroll() { return P == 2 ? 4 : P == 4 ? 2 : 1; }
 
-template <typename T, int P, bool HOP = false>
+template <typename T, int P, bool HOP = false, int U = 1>
 __global__ void __launch_bounds__(kThreads) k_fused_reduce_ldst(const __grid_constant__ FusedArgs a) {
   pdl_trigger();
   pdl_wait();
@@ -78,10 +78,9 @@ __global__ void __launch_bounds__(kThreads) k_fused_reduce_ldst(const __grid_con
     }
   }
 
-  if constexpr (P > 0 && ldst_unroll<P>() > 1) {
+  if constexpr (P > 0 && U > 1) {
     // block b takes vectors [b * U * blockDim, (b + 1) * U * blockDim) of the chunk;
     // all U * P loads are issued before the first fold
-    constexpr int U = ldst_unroll<P>();
     const int64_t bstride = static_cast<int64_t>(gridDim.x) * blockDim.x * U;
     for (int64_t v0 = static_cast<int64_t>(blockIdx.x) * blockDim.x * U + threadIdx.x; v0 < nvec; v0 += bstride) {
       uint4 x[U][P];
@@ -634,18 +633,31 @@ int fused_blocks_per_chunk(int64_t vectors, int per_block) {
   return static_cast<int>(bx);
 }
 
+// The unrolled form only while its grid still holds 4 blocks per SM: on
+// small chunks, more blocks beat more loads per thread.
+template <typename T, int P, bool HOP>
+cudaError_t launch_ldst(const FusedArgs& a, cudaStream_t s) {
+  constexpr int V = Vec<T>::N;
+  constexpr int UP = ldst_unroll<P>();
+  const int64_t vectors = a.cs / V + 1;
+  if constexpr (UP > 1) {
+    const int bx = fused_blocks_per_chunk(vectors, kThreads * UP);
+    if (static_cast<int64_t>(bx) * a.p >= 4 * static_cast<int64_t>(sm_count()))
+      return launch_pdl(k_fused_reduce_ldst<T, P, HOP, UP>, dim3(bx, a.p), dim3(kThreads), 0, s, a);
+  }
+  return launch_pdl(k_fused_reduce_ldst<T, P, HOP, 1>, dim3(fused_blocks_per_chunk(vectors, kThreads), a.p),
+                    dim3(kThreads), 0, s, a);
+}
+
 template <typename T, bool HOP>
 cudaError_t fused_ldst(const FusedArgs& a, cudaStream_t s) {
-  constexpr int V = Vec<T>::N;
-  const int U = a.p == 2 ? ldst_unroll<2>() : a.p == 4 ? ldst_unroll<4>() : 1;
-  const dim3 grid(fused_blocks_per_chunk(a.cs / V + 1, kThreads * U), a.p);
   cudaError_t e;
   switch (a.p) {
-    case 2: e = launch_pdl(k_fused_reduce_ldst<T, 2, HOP>, grid, dim3(kThreads), 0, s, a); break;
-    case 4: e = launch_pdl(k_fused_reduce_ldst<T, 4, HOP>, grid, dim3(kThreads), 0, s, a); break;
-    case 8: e = launch_pdl(k_fused_reduce_ldst<T, 8, HOP>, grid, dim3(kThreads), 0, s, a); break;
-    case 16: e = launch_pdl(k_fused_reduce_ldst<T, 16, HOP>, grid, dim3(kThreads), 0, s, a); break;
-    default: e = launch_pdl(k_fused_reduce_ldst<T, 0, HOP>, grid, dim3(kThreads), 0, s, a); break;
+    case 2: e = launch_ldst<T, 2, HOP>(a, s); break;
+    case 4: e = launch_ldst<T, 4, HOP>(a, s); break;
+    case 8: e = launch_ldst<T, 8, HOP>(a, s); break;
+    case 16: e = launch_ldst<T, 16, HOP>(a, s); break;
+    default: e = launch_ldst<T, 0, HOP>(a, s); break;
   }
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
