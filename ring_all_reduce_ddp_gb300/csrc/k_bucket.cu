@@ -73,11 +73,28 @@ __device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divi
   void* const* rep = a.ptr + static_cast<int64_t>(a.slot[i]) * p;
   const int o = a.origin[i];
 
-  T* base[P > 0 ? P : 1];  // replicas in ring order o, o+1, ... (mod p)
+  // The replicas in ring order o, o+1, ... (mod p). fp32 holds them in
+  // registers. bf16, launched one block per tile, stages them in shared
+  // memory, which takes the kernel from 74 to 40 registers. Measured on GB300,
+  // back to back: the bf16 Llama-1B set's sync 5,748 -> 5,676 us; on the fp32
+  // sets, with their persistent grid, shared memory was 2 % slower.
+  constexpr bool kSharedBases = sizeof(T) == 2;
+  __shared__ T* s_base[P > 0 ? P : 1];
+  T* r_base[P > 0 ? P : 1];
   if constexpr (P > 0) {
+    if constexpr (kSharedBases) {
+      __syncthreads();  // every thread is done with the previous tile's bases
+      if (threadIdx.x < P) s_base[threadIdx.x] = reinterpret_cast<T*>(rep[(o + threadIdx.x) % P]);
+      __syncthreads();
+    } else {
 #pragma unroll
-    for (int j = 0; j < P; ++j) base[j] = reinterpret_cast<T*>(rep[(o + j) % P]);
+      for (int j = 0; j < P; ++j) r_base[j] = reinterpret_cast<T*>(rep[(o + j) % P]);
+    }
   }
+  auto base = [&](int j) -> T* {
+    if constexpr (kSharedBases) return s_base[j];
+    else return r_base[j];
+  };
 
   wait_previous_grid(waited);
 
@@ -109,7 +126,7 @@ __device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divi
     if constexpr (P > 0) {
       uint4 w[P];
 #pragma unroll
-      for (int j = 0; j < P; ++j) w[j] = ld_prefetch256(base[j] + x);
+      for (int j = 0; j < P; ++j) w[j] = ld_prefetch256(base(j) + x);
       Vec<T>::unpack(w[0], acc);
 #pragma unroll
       for (int j = 1; j < P; ++j) {
@@ -122,7 +139,7 @@ __device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divi
       for (int l = 0; l < V; ++l) acc[l] = __fdiv_rn(acc[l], divisor);
       const uint4 y = Vec<T>::pack(acc);
 #pragma unroll
-      for (int q = 0; q < P; ++q) *reinterpret_cast<uint4*>(base[q] + x) = y;
+      for (int q = 0; q < P; ++q) *reinterpret_cast<uint4*>(base(q) + x) = y;
     } else {
       Vec<T>::unpack(*reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(rep[o]) + x), acc);
       int r = o;
