@@ -134,16 +134,15 @@ struct StagedArgs {
 // summation origin (its chunk index). ptr[slot * p + r] is replica r's tensor
 // in local slot `slot`; piece i covers elements [start, start + len) of that
 // tensor; tile0 is the prefix of each piece's tiles of bucket_tile_elems
-// elements. Tile bytes per replica, measured on GB300 over the ResNet-50,
-// GPT-2 and Llama-1B-shaped gradient sets: 16 KB for fp32 (8 and 32 KB were
-// slower), 64 KB for bf16 (1 % faster than 16 KB).
+// elements. A tile is 4 KB per replica: one 16-byte vector per thread of a
+// 256-thread block, one block per tile. Measured on GB300 that way on the
+// ResNet-50-shaped set: 4, 8, 16, 32 and 64 KB tiles took 244.4, 246.6,
+// 250.4, 259.4 and 264.1 us; on the bf16 Llama-1B set 4 KB beat 8 and 64 KB
+// (5,499, 5,517 and 5,677 us).
 constexpr int kBucketPtrs = 1024;
 constexpr int kBucketPieces = 256;
-constexpr int kBucketTileBytes = 16384;
-constexpr int kBucketTileBytesBf16 = 65536;
-__host__ __device__ constexpr int64_t bucket_tile_elems(int elem_size) {
-  return elem_size == 2 ? kBucketTileBytesBf16 / 2 : kBucketTileBytes / elem_size;
-}
+constexpr int kBucketTileBytes = 4096;
+__host__ __device__ constexpr int64_t bucket_tile_elems(int elem_size) { return kBucketTileBytes / elem_size; }
 struct BucketArgs {
   void* ptr[kBucketPtrs];
   int64_t start[kBucketPieces];

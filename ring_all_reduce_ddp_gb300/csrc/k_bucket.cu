@@ -11,9 +11,7 @@
 // ((x_c + x_{c+1}) + ...) + x_{c+p-1}, then divided once by the divisor: the
 // same bits as the ring on the flat bucket. Work is cut into pieces (a tensor
 // intersected with a chunk: one origin each) and pieces into tiles of
-// bucket_tile_elems elements per replica; blocks stride over the tiles.
-#include <atomic>
-
+// bucket_tile_elems elements per replica; one block per tile.
 #include "launch.h"
 
 namespace ddp {
@@ -73,28 +71,19 @@ __device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divi
   void* const* rep = a.ptr + static_cast<int64_t>(a.slot[i]) * p;
   const int o = a.origin[i];
 
-  // The replicas in ring order o, o+1, ... (mod p). fp32 holds them in
-  // registers. bf16, launched one block per tile, stages them in shared
-  // memory, which takes the kernel from 74 to 40 registers. Measured on GB300,
-  // back to back: the bf16 Llama-1B set's sync 5,748 -> 5,676 us; on the fp32
-  // sets, with their persistent grid, shared memory was 2 % slower.
-  constexpr bool kSharedBases = sizeof(T) == 2;
-  __shared__ T* s_base[P > 0 ? P : 1];
-  T* r_base[P > 0 ? P : 1];
+  // The replicas in ring order o, o+1, ... (mod p), staged in shared memory
+  // rather than held in registers: 40 registers instead of 74 at p = 8, so six
+  // blocks fit on an SM instead of three, which is what hides each tile's
+  // table lookups. Measured on GB300, one block per 4 KB tile against the
+  // earlier persistent grid over 16 KB tiles with the pointers in registers:
+  // ResNet-50-shaped sync 258.7 -> 244.4 us, GPT-2 1,222 -> 1,142 us, bf16
+  // Llama-1B 5,678 -> 5,499 us.
+  __shared__ T* base[P > 0 ? P : 1];
   if constexpr (P > 0) {
-    if constexpr (kSharedBases) {
-      __syncthreads();  // every thread is done with the previous tile's bases
-      if (threadIdx.x < P) s_base[threadIdx.x] = reinterpret_cast<T*>(rep[(o + threadIdx.x) % P]);
-      __syncthreads();
-    } else {
-#pragma unroll
-      for (int j = 0; j < P; ++j) r_base[j] = reinterpret_cast<T*>(rep[(o + j) % P]);
-    }
+    __syncthreads();  // every thread is done with the previous tile's bases
+    if (threadIdx.x < P) base[threadIdx.x] = reinterpret_cast<T*>(rep[(o + threadIdx.x) % P]);
+    __syncthreads();
   }
-  auto base = [&](int j) -> T* {
-    if constexpr (kSharedBases) return s_base[j];
-    else return r_base[j];
-  };
 
   wait_previous_grid(waited);
 
@@ -126,7 +115,7 @@ __device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divi
     if constexpr (P > 0) {
       uint4 w[P];
 #pragma unroll
-      for (int j = 0; j < P; ++j) w[j] = ld_prefetch256(base(j) + x);
+      for (int j = 0; j < P; ++j) w[j] = ld_prefetch256(base[j] + x);
       Vec<T>::unpack(w[0], acc);
 #pragma unroll
       for (int j = 1; j < P; ++j) {
@@ -139,7 +128,7 @@ __device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divi
       for (int l = 0; l < V; ++l) acc[l] = __fdiv_rn(acc[l], divisor);
       const uint4 y = Vec<T>::pack(acc);
 #pragma unroll
-      for (int q = 0; q < P; ++q) *reinterpret_cast<uint4*>(base(q) + x) = y;
+      for (int q = 0; q < P; ++q) *reinterpret_cast<uint4*>(base[q] + x) = y;
     } else {
       Vec<T>::unpack(*reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(rep[o]) + x), acc);
       int r = o;
@@ -181,43 +170,19 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce_table(const Bucke
   bucket_tiles<T, P>(v, divisor);
 }
 
-// fp32: a persistent grid, as many blocks as fit on the device at once (at most
-// one per tile); the occupancy of each kernel instantiation is looked up once
-// per device. bf16: one block per tile. Measured on GB300, back to back on the
-// model-shaped syncs: on the fp32 ResNet-50 and GPT-2 sets the persistent grid
-// is 1.5-3.5 % faster; on the bf16 Llama-1B set one block per 64 KB tile takes
-// 5,759 us against 5,904 us.
-template <typename T, int P, bool kTable>
-int persistent_grid(int32_t tiles) {
-  if constexpr (sizeof(T) == 2) return tiles;
-  static std::atomic<int> per_sm[64];  // zero-initialised (static storage)
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  int cached = per_sm[dev].load(std::memory_order_relaxed);
-  if (cached == 0) {
-    int blocks = 0;
-    cudaError_t e;
-    if constexpr (kTable)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_bucket_allreduce_table<T, P>, kThreads, 0);
-    else
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_bucket_allreduce<T, P>, kThreads, 0);
-    cached = (e == cudaSuccess && blocks > 0) ? blocks : 1;
-    per_sm[dev].store(cached, std::memory_order_relaxed);
-  }
-  const int64_t g = static_cast<int64_t>(cached) * sm_count();
-  return static_cast<int>(g < tiles ? g : tiles);
-}
-
+// One block per tile: blocks are dispatched in index order, so the resident
+// ones work on consecutive tiles. Measured on GB300 and slower: a persistent
+// grid striding over the tiles, and one taking tiles in order from a device
+// counter.
 template <typename T>
 cudaError_t by_value(const BucketArgs& a, cudaStream_t s) {
   const int32_t tiles = a.tile0[a.npieces];
   switch (a.p) {
-    case 2: k_bucket_allreduce<T, 2><<<persistent_grid<T, 2, false>(tiles), kThreads, 0, s>>>(a); break;
-    case 4: k_bucket_allreduce<T, 4><<<persistent_grid<T, 4, false>(tiles), kThreads, 0, s>>>(a); break;
-    case 8: k_bucket_allreduce<T, 8><<<persistent_grid<T, 8, false>(tiles), kThreads, 0, s>>>(a); break;
-    case 16: k_bucket_allreduce<T, 16><<<persistent_grid<T, 16, false>(tiles), kThreads, 0, s>>>(a); break;
-    default: k_bucket_allreduce<T, 0><<<persistent_grid<T, 0, false>(tiles), kThreads, 0, s>>>(a); break;
+    case 2: k_bucket_allreduce<T, 2><<<tiles, kThreads, 0, s>>>(a); break;
+    case 4: k_bucket_allreduce<T, 4><<<tiles, kThreads, 0, s>>>(a); break;
+    case 8: k_bucket_allreduce<T, 8><<<tiles, kThreads, 0, s>>>(a); break;
+    case 16: k_bucket_allreduce<T, 16><<<tiles, kThreads, 0, s>>>(a); break;
+    default: k_bucket_allreduce<T, 0><<<tiles, kThreads, 0, s>>>(a); break;
   }
   count_launch();
   return cudaGetLastError();
@@ -231,7 +196,7 @@ cudaError_t by_value(const BucketArgs& a, cudaStream_t s) {
 template <typename T, int P>
 cudaError_t launch_table(const BucketTable& t, int32_t tiles, float divisor, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(persistent_grid<T, P, true>(tiles));
+  cfg.gridDim = dim3(tiles);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
