@@ -228,6 +228,18 @@ def algo_code(name):
             "ring_steps": D.DDP_ALGO_RING_STEPS}[name]
 
 
+def l2_note(grad_bytes: int, dev: int) -> str:
+    """What the timed steps find in L2: the gradients of every replica are
+    read and written once per step, so above twice the L2 size no step can
+    find the previous step's data there."""
+    import torch
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20)
+    if grad_bytes > 2 * l2:
+        return "inputs larger than L2: %.2f GB of gradients per step, L2 %.0f MB" % (grad_bytes / 1e9, l2 / 1e6)
+    return ("inputs fit in L2: %.1f MB of gradients per step, L2 %.0f MB; steps run L2-warm, so this "
+            "workload measures latency, not HBM bandwidth" % (grad_bytes / 1e6, l2 / 1e6))
+
+
 def kernel_sha() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -486,8 +498,7 @@ def run_ours(args, ranks: Ranks):
         "config": {"workload": WORKLOAD_TEXT[args.config], "p": p, "buckets": nb, "bucket_mb": bucket_mb,
                    "algo": args.algo, "sync": "in_place" if mode == D.DDP_SYNC_IN_PLACE else "flatten",
                    "divisor": divisor,
-                   "l2": "inputs larger than L2: %.2f GB of gradients per step" %
-                         (sum(a.numel() * a.element_size() for a in arenas) / 1e9),
+                   "l2": l2_note(sum(a.numel() * a.element_size() for a in arenas), dev),
                    "parallelism": f"replicas only: {ranks.world} independent GPU(s)"},
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
