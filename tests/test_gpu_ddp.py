@@ -268,11 +268,14 @@ def test_tiny_ddp_sync_full_parity(algo, mode, dtype):
     assert D.ddp_device_error() == 0
 
 
+@pytest.mark.parametrize("skew", [False, True])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("p", [1, 2, 3, 4, 8, 16, 17, 64])
-def test_bucket_allreduce_in_place_matches_flatten_path_oracle(p, dtype):
+def test_bucket_allreduce_in_place_matches_flatten_path_oracle(p, dtype, skew):
     """One bucket of odd tensors (some spanning several chunks, some inside one,
-    a zero-size one, misaligned offsets) reduced straight on the gradients."""
+    a zero-size one, misaligned offsets) reduced straight on the gradients.
+    With skew, a tensor's start differs between replicas mod 16 bytes, so its
+    tiles take the scalar path."""
     rng = np.random.default_rng(p)
     sizes = [int(x) for x in rng.integers(0, 3000, size=12)] + [0, 1, 5, 40000]
     order = list(range(len(sizes)))[::-1]
@@ -289,7 +292,8 @@ def test_bucket_allreduce_in_place_matches_flatten_path_oracle(p, dtype):
         row, hrow = [], []
         for t, sz in enumerate(sizes):
             base = torch.empty(sz + 3, dtype=tdt, device="cuda")
-            v = base[(t % 3):(t % 3) + sz]  # misaligned starts, the same on every replica
+            sh = (t + r) % 3 if skew else t % 3  # misaligned starts, the same on every replica unless skewed
+            v = base[sh:sh + sz]
             if sz:
                 synth.fill_(v, "normal", 77, r * 100 + t)
             row.append(v)
