@@ -268,6 +268,36 @@ def test_tiny_ddp_sync_full_parity(algo, mode, dtype):
     assert D.ddp_device_error() == 0
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("algo,mode", SYNCS)
+def test_tiny_ddp_sync_replicas_misaligned_differently(algo, mode, dtype):
+    """The tiny set with each tensor moved 0-2 elements off its allocation's
+    start, by an amount that differs between replicas: the in-place sync's
+    tiles, whose replicas then differ mod 16 bytes, take the scalar path."""
+    cfg = dict(W.CONFIGS["tiny"], dtype=dtype)
+    p = cfg["p"]
+    src, _ = W.make_grads(cfg)
+    keep, grads = [], []
+    for r in range(p):
+        row = []
+        for t, g in enumerate(src[r]):
+            base = torch.empty(g.numel() + 3, dtype=g.dtype, device="cuda")
+            sh = (t + r) % 3
+            v = base[sh:sh + g.numel()]
+            v.copy_(g.view(-1))
+            keep.append(base)
+            row.append(v.view(g.shape))
+        grads.append(row)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    red.sync_gradients(W.divisor(cfg), algo, mode)
+    torch.cuda.synchronize()
+    want = _tiny_expected(cfg, red)
+    for r in range(p):
+        for t in range(len(grads[r])):
+            assert_bit_equal(to_host(grads[r][t]), want[r][t], f"tensor {t} replica {r}")
+    assert D.ddp_device_error() == 0
+
+
 @pytest.mark.parametrize("skew", [False, True])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("p", [1, 2, 3, 4, 8, 16, 17, 64])
