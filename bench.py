@@ -578,6 +578,32 @@ def run_reference(args, ranks: Ranks):
     print(json.dumps(line), flush=True)
 
 # --------------------------------------------------------------- sweep
+def literal_traffic_bytes(op: str, algo: str, p: int, M: int):
+    """HBM bytes one literal (launch-per-step) fp32 schedule moves, counted from
+    its kernels, for the sweep's actual-traffic rate; None for the fused forms
+    and the tree-shaped schedules. M is the sweep size in bytes.
+    - all-reduce: p-1 reduce-scatter steps that read the local and the received
+      chunk and write the sum (3 x 4 bytes per element, n elements per step
+      over all ranks), then p-1 all-gather steps that copy one chunk per rank
+      (2 x 4 bytes per element): 5(p-1) M;
+    - reduce-scatter: p-1 steps of 3 x 4 bytes per element (inputs and fp32
+      partials in, partials or the output out): 3(p-1) M;
+    - all-gather of M / p bytes per rank into M: the placement copy and p-1
+      steps, each copying M / p bytes on every rank: 2 p M;
+    - broadcast by the doubling tree: p-1 copies of M: 2(p-1) M."""
+    if algo != "ring_steps" or p < 2:
+        return None
+    if op == "allreduce":
+        return 5 * (p - 1) * M
+    if op.startswith("reduce_scatter"):
+        return 3 * (p - 1) * M
+    if op == "allgather":
+        return 2 * p * M
+    if op == "broadcast":
+        return 2 * (p - 1) * M
+    return None
+
+
 def run_sweep(args, ranks: Ranks):
     """Message-size / rank-count sweep: one fp32 buffer of M = 1 KiB * 4^k bytes
     on each of p replicas (p * M <= 64 GiB), values uniform on [-1, 1);
@@ -711,10 +737,13 @@ def run_sweep(args, ranks: Ranks):
                         del g
                     t = t_graph if t_graph is not None else t_eager
                     gbs = nbytes / t / 1e9
+                    moved = literal_traffic_bytes(op, an, p, M)
                     line = {"sweep": op, "algo": an, "p": p, "bytes": M, "us": round(t * 1e6, 2),
                             "us_eager": round(t_eager * 1e6, 2), "timing": "graph" if t_graph else "eager",
                             "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
                             "busbw_gbs": round(M / t / 1e9 * 2 * (p - 1) / p, 1) if op == "allreduce" else None,
+                            "traffic_gbs": round(moved / t / 1e9, 1) if moved else None,
+                            "traffic_frac": round(moved / t / 1e9 / peak, 4) if moved else None,
                             "input_copies": nsets, "reps": nrep, "batches": nbat}
                     print(json.dumps(line), flush=True)
             del sets
