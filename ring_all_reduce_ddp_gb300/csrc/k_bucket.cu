@@ -158,6 +158,7 @@ __device__ __forceinline__ void bucket_tiles(const View& v, float divisor) {
 // Arguments by value (one bucket, from ddp_bucket_allreduce).
 template <typename T, int P>
 __global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_constant__ BucketArgs a) {
+  pdl_trigger();
   const View v{a.ptr, a.start, a.len, a.slot, a.origin, a.tile0, a.npieces, a.p};
   bucket_tiles<T, P>(v, a.divisor);
 }
@@ -173,19 +174,22 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce_table(const Bucke
 // One block per tile: blocks are dispatched in index order, so the resident
 // ones work on consecutive tiles. Measured on GB300 and slower: a persistent
 // grid striding over the tiles, and one taking tiles in order from a device
-// counter.
+// counter. Each bucket's launch is a programmatic dependent of the previous
+// kernel in the stream (usually the previous bucket's), so its blocks start
+// while that kernel's last wave drains.
 template <typename T>
 cudaError_t by_value(const BucketArgs& a, cudaStream_t s) {
-  const int32_t tiles = a.tile0[a.npieces];
+  const dim3 grid(a.tile0[a.npieces]), block(kThreads);
+  cudaError_t e;
   switch (a.p) {
-    case 2: k_bucket_allreduce<T, 2><<<tiles, kThreads, 0, s>>>(a); break;
-    case 4: k_bucket_allreduce<T, 4><<<tiles, kThreads, 0, s>>>(a); break;
-    case 8: k_bucket_allreduce<T, 8><<<tiles, kThreads, 0, s>>>(a); break;
-    case 16: k_bucket_allreduce<T, 16><<<tiles, kThreads, 0, s>>>(a); break;
-    default: k_bucket_allreduce<T, 0><<<tiles, kThreads, 0, s>>>(a); break;
+    case 2: e = launch_pdl(k_bucket_allreduce<T, 2>, grid, block, 0, s, a); break;
+    case 4: e = launch_pdl(k_bucket_allreduce<T, 4>, grid, block, 0, s, a); break;
+    case 8: e = launch_pdl(k_bucket_allreduce<T, 8>, grid, block, 0, s, a); break;
+    case 16: e = launch_pdl(k_bucket_allreduce<T, 16>, grid, block, 0, s, a); break;
+    default: e = launch_pdl(k_bucket_allreduce<T, 0>, grid, block, 0, s, a); break;
   }
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // The whole-Reducer launch may start while the previous kernel in the stream

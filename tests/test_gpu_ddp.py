@@ -427,3 +427,42 @@ def test_sync_reads_what_the_kernel_before_it_wrote(name):
         for r in range(1, p):
             assert torch.equal(grads[r][t].view(torch.int32), grads[0][t].view(torch.int32))
     assert D.ddp_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "resnet50"])
+def test_ready_firing_reads_what_the_kernel_before_it_wrote(name):
+    """Readiness-driven firing launches each bucket as a programmatic dependent
+    of the kernel before it: the coalesced broadcast that writes the gradients,
+    then the previous bucket. Every bucket must reduce the broadcast values."""
+    cfg = W.CONFIGS[name]
+    p = cfg["p"]
+    grads, _ = W.make_grads(cfg)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    numel = W.numels(cfg)
+    starts = W.tensor_starts(cfg)
+    s = torch.cuda.current_stream()
+    Dv = W.divisor(cfg)
+    for rep in range(3):
+        broadcast_buffers(grads, 0, 0, D.DDP_ALGO_FUSED, s)
+        red.prepare()
+        fired = sum(red.mark_ready(t, Dv, None, s) for t in range(len(numel) - 1, -1, -1))
+        assert fired == len(red.buckets)
+        if rep == 0:
+            torch.cuda.synchronize()
+            rng = np.random.default_rng(12)
+            for members in red.buckets:
+                for t in members:
+                    idx = np.unique(np.concatenate([np.arange(min(64, numel[t])),
+                                                    rng.integers(0, numel[t], size=min(256, numel[t]))]))
+                    x0 = W.host_values(cfg, 0, starts[t] + idx)
+                    acc = x0.copy()
+                    for _ in range(p - 1):
+                        acc = (acc + x0).astype(np.float32)
+                    want = (acc / np.float32(Dv)).astype(np.float32)
+                    for r in range(p):
+                        assert_bit_equal(to_host(grads[r][t])[idx], want, f"tensor {t} replica {r}")
+    torch.cuda.synchronize()
+    for t in range(len(numel)):
+        for r in range(1, p):
+            assert torch.equal(grads[r][t].view(torch.int32), grads[0][t].view(torch.int32))
+    assert D.ddp_device_error() == 0
