@@ -26,3 +26,33 @@ def test_peak_and_workload_text():
     peak, kind = bench.peak_hbm()
     assert peak > 1000 and kind in ("measured", "fallback")
     assert "ResNet-50" in bench.WORKLOAD_TEXT["resnet50"]
+
+
+def test_literal_traffic_counts_match_the_schedule():
+    """The sweep's load-and-store byte counts for the literal schedules, counted
+    here access by access over the steps (chunks from the oracle's plan)."""
+    from oracle.ring import chunk_bounds
+    for p in range(2, 10):
+        n = 1024 * p  # the sweep's sizes divide by every p it uses
+        M = 4 * n
+        chunks = chunk_bounds(n, p)
+        # all-reduce: every reduce-scatter step, each rank loads its chunk and the
+        # received one and stores the sum; every all-gather step, each rank
+        # loads one chunk and stores it at its neighbour
+        rs = sum(3 * 4 * (hi - lo) for _ in range(p - 1) for lo, hi in chunks)
+        ag = sum(2 * 4 * (hi - lo) for _ in range(p - 1) for lo, hi in chunks)
+        assert bench.literal_traffic_bytes("allreduce", "ring_steps", p, M) == rs + ag
+        assert bench.literal_traffic_bytes("reduce_scatter_rank", "ring_steps", p, M) == rs
+        # all-gather of n / p elements per rank: a placement copy, then p - 1 steps
+        m = n // p
+        assert bench.literal_traffic_bytes("allgather", "ring_steps", p, M) == 2 * 4 * m * p * p
+        # doubling tree: every rank but the root receives one copy of M bytes
+        copies = 0
+        span = 1
+        while span < p:
+            copies += sum(1 for v in range(span) if v + span < p)
+            span *= 2
+        assert copies == p - 1
+        assert bench.literal_traffic_bytes("broadcast", "ring_steps", p, M) == 2 * copies * M
+    assert bench.literal_traffic_bytes("allreduce", "fused", 8, 1 << 20) is None
+    assert bench.literal_traffic_bytes("allreduce", "rd", 8, 1 << 20) is None
