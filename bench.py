@@ -4,10 +4,11 @@ held in one GPU's memory.
 
 A step is one pass of the whole hot path on the workload's synthetic
 gradients: bucket assignment (host), the per-forward coalesced broadcast of the
-model's buffers from replica 0, then the gradient sync of every bucket. By
-default (--mode in_place) the sync is one launch that, for every bucket,
-flattens, ring-all-reduces and unflattens in a single pass over the
-gradients; --mode flatten runs the three separate kernels per bucket.
+model's buffers from replica 0, and the gradient sync of every bucket. By
+default (--mode in_place) the broadcast and the sync are ONE launch: every
+bucket is flattened, ring-all-reduced and unflattened in a single pass over
+the gradients, and the buffers are copied in the same grid. --mode flatten
+runs the broadcast, then the three separate kernels per bucket.
 
 Default workload: the ResNet-50-shaped gradient set (161 fp32 tensors, 25.6M
 parameters) on p = 8 replicas, 1 MiB first bucket / 25 MiB buckets, averaged
@@ -15,8 +16,11 @@ by 1/8, plus the broadcast of its 159 BatchNorm buffers.
 
 Prints ONE JSON line (rank 0). value = algorithmic bytes of all the step's ops
 (all-reduce 2pM; in flatten mode also flatten 2pM and unflatten 2pM; broadcast
-p * buffer bytes) over the device-timed step, in GB/s, summed over ranks. --impl reference times the
-CPU oracle instead (on a bounded sample of the same workload).
+p * buffer bytes) over the device-timed step, in GB/s, summed over ranks. The
+same line carries the dominant kernel's roofline over a separate pass of 64
+back-to-back launches, the message-size / rank-count points of the fused
+all-reduce (`sweep`) and the GPT-2 and Llama-1B gradient sets (`configs`).
+--impl reference times the CPU oracle instead, on the same step.
 """
 from __future__ import annotations
 
@@ -51,7 +55,7 @@ WORKLOAD_TEXT = {
 # DRAM traffic of the dominant kernel (the in-place bucket all-reduce) from an
 # ncu capture, as bytes per algorithmic byte; valid only while the kernel
 # source it was taken on is unchanged (checked by hash).
-EVENT_EVERY = 16  # timed steps per event-timed launch of the dominant kernel
+ROOFLINE_LAUNCHES = 64  # back-to-back launches of the dominant kernel timed for the roofline
 NCU_TRAFFIC = {"kernel_sha256": "bcda9671e69737c3c345e46175295989edaac7c9ca0e1b38bafa06760dca6851",
                "config": "resnet50",  # the workload the capture ran; other workloads report null
                "dram_bytes_per_algorithmic_byte": (818.002432 + 758.240256) / 1635.650048}  # ncu: read + write MB per launch
@@ -67,7 +71,8 @@ def parse_args():
     ap.add_argument("--algo", default="fused", choices=["fused", "ldst", "tma", "ring_steps"])
     ap.add_argument("--mode", default="in_place", choices=["in_place", "flatten"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--cpu-budget-s", type=float, default=8.0)
+    ap.add_argument("--no-extras", action="store_true", help="leave out the sweep and configs fields")
     ap.add_argument("--sweep", action="store_true", help="message-size / rank-count sweep, one line per point")
     ap.add_argument("--overlap", action="store_true", help="exposed communication vs bucket cap, one line per cap")
     return ap.parse_args()
@@ -250,44 +255,81 @@ def kernel_sha() -> str:
 
 
 # --------------------------------------------------------------- CPU oracle
-def oracle_sync_sample(cfg, budget_s: float, max_buckets=None):
-    """Time the oracle's gradient sync (flatten, literal ring all-reduce,
-    unflatten) bucket by bucket until the budget is used. Returns
-    (algorithmic bytes, seconds, description). Inputs are generated untimed."""
+def oracle_inputs(cfg):
+    """Host copies of the workload's inputs, from the seeded generator (not
+    read from any device): per replica its gradients in registration order,
+    and the per-forward buffers' bytes (None if the workload has none)."""
     import numpy as np
 
+    from synth import workloads as W
+    numel = W.numels(cfg)
+    starts = W.tensor_starts(cfg)
+    grads = [[W.host_values(cfg, r, np.arange(starts[t], starts[t] + numel[t])) for t in range(len(numel))]
+             for r in range(cfg["p"])]
+    bufs = W.buffer_set_host(cfg) if cfg.get("buffers") else None
+    return grads, bufs
+
+
+def oracle_step_bytes(cfg, frac: float = 1.0) -> int:
+    """Algorithmic bytes of one step, counted as the GPU arm counts them: the
+    sync reads and writes every replica's gradients once (2pM), the broadcast
+    reads the root's buffers once and writes the p - 1 others (p B). With
+    frac < 1, the leading frac of every bucket (see oracle_step)."""
+    from oracle import buckets as ob
+    from synth import workloads as W
+    numel = W.numels(cfg)
+    es, p = W.esize(cfg), cfg["p"]
+    plan = ob.assign_buckets(numel, es, cfg["first_cap"], cfg["cap"])
+    _, _, bnumel = ob.bucket_layout(numel, plan)
+    n = sum(bnumel) if frac >= 1 else sum(max(p, int(x * frac)) for x in bnumel)
+    buf = sum(x.size for x in W.buffer_set_host(cfg, p=1)[0]) if cfg.get("buffers") and p > 1 else 0
+    return 2 * p * n * es + p * buf
+
+
+def oracle_step(cfg, grads, bufs, frac: float = 1.0):
+    """One step of the path in the oracle, as it stands: bucket assignment,
+    the coalesced broadcast of the buffers from replica 0, and for every bucket
+    flatten, literal ring all-reduce and unflatten. With frac < 1 (a timing
+    sample when the whole step would take too long) each bucket's all-reduce
+    runs on its leading frac of elements and nothing is unflattened."""
     from oracle import buckets as ob
     from oracle import ring as orc
     from synth import workloads as W
     numel = W.numels(cfg)
-    starts = W.tensor_starts(cfg)
-    es = W.esize(cfg)
     p = cfg["p"]
-    plan = ob.assign_buckets(numel, es, cfg["first_cap"], cfg["cap"])
+    plan = ob.assign_buckets(numel, W.esize(cfg), cfg["first_cap"], cfg["cap"])
     _, offset, bnumel = ob.bucket_layout(numel, plan)
+    if bufs is not None:
+        orc.broadcast_coalesced(bufs, 0)
     Dv = W.divisor(cfg)
-    total_bytes, total_t, done = 0, 0.0, []
     for b, members in enumerate(plan):
-        if max_buckets is not None and len(done) >= max_buckets:
-            break
-        grads = [{t: W.host_values(cfg, r, np.arange(starts[t], starts[t] + numel[t])) for t in members}
-                 for r in range(p)]
+        flats = [ob.flatten(grads[r], members, offset, bnumel[b]) for r in range(p)]
+        if frac >= 1:
+            outs, _ = orc.allreduce(flats, bnumel[b], Dv, cfg["dtype"])
+            for r in range(p):
+                ob.unflatten(outs[r], members, offset, numel)
+        else:
+            m = max(p, int(bnumel[b] * frac))
+            orc.allreduce([f[:m] for f in flats], m, Dv, cfg["dtype"])
+
+
+def oracle_baseline(cfg, budget_s: float):
+    """The oracle's whole step on the host, single thread, timed step by step
+    until the budget is used (at least one step). Inputs are made untimed."""
+    grads, bufs = oracle_inputs(cfg)
+    times = []
+    while not times or sum(times) < budget_s:
         t0 = time.perf_counter()
-        flats = []
-        for r in range(p):
-            flats.append(ob.flatten([grads[r].get(t, np.zeros(0, np.float32 if es == 4 else np.uint16))
-                                     for t in range(len(numel))], members, offset, bnumel[b]))
-        outs, _ = orc.allreduce(flats, bnumel[b], Dv, cfg["dtype"])
-        for r in range(p):
-            ob.unflatten(outs[r], members, offset, numel)
-        total_t += time.perf_counter() - t0
-        total_bytes += 3 * 2 * p * bnumel[b] * es
-        done.append(b)
-        if total_t >= budget_s:
-            break
-    desc = (f"oracle flatten + literal ring all-reduce + unflatten of buckets {done} "
-            f"({sum(bnumel[b] for b in done)} of {sum(bnumel)} elements per replica, p={p}), single thread")
-    return total_bytes, total_t, desc
+        oracle_step(cfg, grads, bufs)
+        times.append(time.perf_counter() - t0)
+    nbytes = oracle_step_bytes(cfg)
+    return {"value": round(nbytes * len(times) / sum(times) / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "ms_per_step": round(1e3 * statistics.mean(times), 1), "steps": len(times),
+            "sample": (f"the whole step in the oracle, {len(times)} time(s): bucket assignment, coalesced "
+                       f"broadcast of the buffers, flatten + literal ring all-reduce + unflatten of every bucket "
+                       f"(all {cfg['p']} replicas, every element); single thread; bytes counted as the GPU "
+                       f"arm counts them (2pM + pB)"),
+            "host_cores_available": cores_used(), "cpu_model": cpu_model()}
 
 
 # --------------------------------------------------------------- our arm
@@ -308,32 +350,32 @@ def run_ours(args, ranks: Ranks):
     mode = D.DDP_SYNC_IN_PLACE if args.mode == "in_place" else D.DDP_SYNC_FLATTEN
     if args.algo == "ring_steps":
         mode = D.DDP_SYNC_FLATTEN
+    one_launch = mode == D.DDP_SYNC_IN_PLACE
     grads, arenas = W.make_grads(cfg, f"cuda:{dev}")
     bufs = W.buffer_set(cfg, f"cuda:{dev}") if cfg.get("buffers") else None
     red = Reducer(grads, cfg["first_cap"], cfg["cap"])
     bsync = BufferSync(bufs, 0) if bufs else None
+    if bufs and one_launch:
+        red.set_buffers(bufs, 0)
     divisor = W.divisor(cfg)
     stream = torch.cuda.current_stream()
     bc_algo = D.DDP_ALGO_RING_STEPS if args.algo == "ring_steps" else D.DDP_ALGO_FUSED
     buf_bytes = sum(bsync.nbytes) if bsync else 0
     esz = W.esize(cfg)
 
-    def step(events=None, m=mode):
-        if not red.assign():  # a1: bucket assignment (host)
+    def step(r=red):
+        if not r.assign():  # a1: bucket assignment (host)
             raise RuntimeError("bucket assignment changed")
-        if bsync:             # a9: the forward's buffer broadcast
-            bsync(bc_algo, stream)
-        if events is not None:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        red.sync_gradients(divisor, algo, m, 1.0, stream)  # a2-a8
-        if events is not None:
-            e1 = torch.cuda.Event(enable_timing=True)
-            e1.record(stream)
-            events.append((e0, e1))
+        if one_launch:      # a9 + a2-a8: buffer broadcast and in-place sync, one launch
+            r.step(divisor, stream)
+        else:
+            if bsync:
+                bsync(bc_algo, stream)
+            r.sync_gradients(divisor, algo, mode, 1.0, stream)
 
     ab = red.algorithmic_bytes(mode)
-    step_bytes = ab["total"] + p * buf_bytes
+    bc_bytes = p * buf_bytes if p > 1 else 0
+    step_bytes = ab["total"] + bc_bytes
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize()
@@ -343,16 +385,13 @@ def run_ours(args, ranks: Ranks):
     sampler.start()
     time.sleep(0.3)
     launches0 = D.ddp_kernel_launches()
-    sync_events: list = []
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     ranks.barrier()
     w0 = time.time()
     e0.record(stream)
-    for i in range(args.steps):
-        # the dominant kernel is timed by events around it on every 16th step:
-        # an event pair on every step would add its own cost to the step time
-        step(sync_events if i % EVENT_EVERY == 0 else None)
+    for _ in range(args.steps):
+        step()
     e1.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
@@ -364,35 +403,73 @@ def run_ours(args, ranks: Ranks):
     ms_per_step = ms_max / args.steps
     value = step_bytes * args.steps * ranks.world / (ms_max / 1e3) / 1e9
 
-    # Dominant kernel: the in-place bucket all-reduce, one launch per step over
-    # every bucket. Its duration comes from events recorded around that launch
-    # on its stream (every EVENT_EVERY-th step of the timed region), so any
-    # launch latency the events catch counts against it.
-    sync_ms = [a.elapsed_time(b) for a, b in sync_events]
-    nb = len(red.buckets)
-    launches_per_sync = 1 if mode == D.DDP_SYNC_IN_PLACE else None
-    achieved = ab["allreduce"] * len(sync_ms) / (sum(sync_ms) / 1e3) / 1e9
+    # Dominant kernel: the one-launch step (k_bucket_allreduce_table over the
+    # gradient pieces and the buffers' copy pieces). Its average duration is
+    # taken over ROOFLINE_LAUNCHES launches back to back on its stream, events
+    # around the whole run: each launch reads the gradients the one before it
+    # wrote, 0.8 GB at the default workload, more than L2 holds.
     peak, peak_kind = peak_hbm()
+    roof_launches = ROOFLINE_LAUNCHES
+    kernel_bytes = ab["allreduce"] + (bc_bytes if one_launch else 0)
+
+    def launch():
+        if one_launch:
+            red.step(divisor, stream)
+        else:
+            red.sync_gradients(divisor, algo, mode, 1.0, stream)
+
+    for _ in range(3):
+        launch()
+    torch.cuda.synchronize()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for _ in range(roof_launches):
+        launch()
+    r1.record(stream)
+    torch.cuda.synchronize()
+    avg_us = 1e3 * r0.elapsed_time(r1) / roof_launches
+    achieved = kernel_bytes / (avg_us / 1e6) / 1e9
     traffic = None
     if (NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and NCU_TRAFFIC["config"] == args.config
-            and mode == D.DDP_SYNC_IN_PLACE and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]):
-        traffic = int(NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * ab["allreduce"])
+            and one_launch and NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"]):
+        traffic = int(NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * kernel_bytes)
     bucket_mb = [round(n * esz / 2 ** 20, 2) for n in red.bucket_numel]
-    kernel_name = ("k_bucket_allreduce_table: every bucket's flatten + ring-order all-reduce + unflatten "
-                   "in one launch" if mode == D.DDP_SYNC_IN_PLACE
+    nb = len(red.buckets)
+    kernel_name = ("k_bucket_allreduce_table: every bucket's flatten + ring-order all-reduce + unflatten and the "
+                   "buffers' broadcast in one launch" if one_launch
                    else "flatten, fused all-reduce, unflatten per bucket (whole sync timed)")
+
+    # The same step as two launches (coalesced broadcast, then the in-place
+    # sync), for comparison with the one-launch form.
+    two_launch = None
+    if one_launch and bsync:
+        for _ in range(3):
+            bsync(bc_algo, stream)
+            red.sync_gradients(divisor, algo, mode, 1.0, stream)
+        torch.cuda.synchronize()
+        r0.record(stream)
+        for _ in range(roof_launches):
+            bsync(bc_algo, stream)
+            red.sync_gradients(divisor, algo, mode, 1.0, stream)
+        r1.record(stream)
+        torch.cuda.synchronize()
+        two_launch = {"ms_per_step": round(r0.elapsed_time(r1) / roof_launches, 5), "steps": roof_launches,
+                      "note": "ddp_broadcast_coalesced then ddp_reducer_sync(in place): two launches per step"}
 
     # End to end through the public API: every step copies every replica's
     # gradients in from pinned host memory, synchronises them and copies the
     # result out. Three device copies of the workload rotate, so step i+1's
     # copy-in (H2D stream) never waits for step i's sync: it only needs the
     # copy-out of step i-2, long done. Both link directions stay busy; the
-    # sync runs on the compute stream between them.
+    # step runs on the compute stream between them.
     NSETS = 3
     sets = [(arenas, red)]
     for _ in range(NSETS - 1):
         g_x, a_x = W.make_grads(cfg, f"cuda:{dev}")
-        sets.append((a_x, Reducer(g_x, cfg["first_cap"], cfg["cap"])))
+        r_x = Reducer(g_x, cfg["first_cap"], cfg["cap"])
+        if bufs and one_launch:
+            r_x.set_buffers(bufs, 0)
+        sets.append((a_x, r_x))
     host_in = [a.detach().to("cpu").pin_memory() for a in arenas]
     host_out = [torch.empty_like(h).pin_memory() for h in host_in]
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
@@ -409,11 +486,7 @@ def run_ours(args, ranks: Ranks):
                 a.copy_(h, non_blocking=True)
             h2d_done[k].record(h2d_s)
         stream.wait_event(h2d_done[k])
-        if not red_k.assign():
-            raise RuntimeError("bucket assignment changed")
-        if bsync:
-            bsync(bc_algo, stream)
-        red_k.sync_gradients(divisor, algo, mode, 1.0, stream)
+        step(red_k)
         comp_done[k].record(stream)
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(comp_done[k])
@@ -444,19 +517,17 @@ def run_ours(args, ranks: Ranks):
            "pipeline": "step i's copy-out overlaps step i+1's copy-in (three device copies, three streams)"}
     del sets
 
-    # the same step body (buffer broadcast + sync) captured once as a CUDA graph
-    # and replayed: what host launch overhead costs the eager step
+    # the same step body captured once as a CUDA graph and replayed: what host
+    # launch overhead costs the eager step
     graph = None
-    if mode == D.DDP_SYNC_IN_PLACE and ranks.world == 1:
+    if one_launch and ranks.world == 1:
         cg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cg):
-            if bsync:
-                bsync(bc_algo, None)
-            red.sync_gradients(divisor, algo, mode, 1.0, None)
+            red.step(divisor, None)
         for _ in range(3):
             cg.replay()
         torch.cuda.synchronize()
-        k_g = min(args.steps, 2000)
+        k_g = max(roof_launches, min(args.steps, 2000))
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         g0.record(stream)
         for _ in range(k_g):
@@ -464,118 +535,288 @@ def run_ours(args, ranks: Ranks):
         g1.record(stream)
         torch.cuda.synchronize()
         graph = {"ms_per_step": round(g0.elapsed_time(g1) / k_g, 5), "steps": k_g,
-                 "note": "buffer broadcast + in-place sync replayed from one CUDA graph (bucket assignment stays on the host)"}
+                 "note": "the one-launch step replayed from a CUDA graph (bucket assignment stays on the host)"}
         del cg
 
-    # the three-kernel form of the same step, for comparison (not the headline)
+    # the flatten form of the same step, for comparison (not the headline)
     other = None
-    if mode == D.DDP_SYNC_IN_PLACE:
-        k2 = max(10, args.steps // 5)
+    if one_launch:
+        k2 = max(10, min(args.steps, 200))
+
+        def flat_step():
+            if bsync:
+                bsync(bc_algo, stream)
+            red.sync_gradients(divisor, algo, D.DDP_SYNC_FLATTEN, 1.0, stream)
+
         for _ in range(3):
-            step(None, D.DDP_SYNC_FLATTEN)
+            flat_step()
         torch.cuda.synchronize()
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         g0.record(stream)
         for _ in range(k2):
-            step(None, D.DDP_SYNC_FLATTEN)
+            flat_step()
         g1.record(stream)
         torch.cuda.synchronize()
-        fl = red.algorithmic_bytes(D.DDP_SYNC_FLATTEN)["total"] + p * buf_bytes
+        fl = red.algorithmic_bytes(D.DDP_SYNC_FLATTEN)["total"] + bc_bytes
         ms2 = g0.elapsed_time(g1) / k2
-        other = {"mode": "flatten + all-reduce + unflatten", "ms_per_step": round(ms2, 5),
+        other = {"mode": "broadcast, then flatten + all-reduce + unflatten per bucket", "ms_per_step": round(ms2, 5),
                  "gbs": round(fl / (ms2 / 1e3) / 1e9, 1), "steps": k2}
+
+    extras = {}
+    if one_launch and ranks.world == 1 and args.config == "resnet50" and not args.no_extras:
+        del red, grads, arenas
+        torch.cuda.empty_cache()
+        extras["sweep"] = bench_sweep_points(peak)
+        extras["configs"] = bench_config_points(peak)
 
     cpu = None
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
-        nbytes, secs, desc = oracle_sync_sample(cfg, args.cpu_budget_s)
-        cpu = {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
-               "host_cores_available": cores_used(), "cpu_model": cpu_model()}
+        cpu = oracle_baseline(cfg, args.cpu_budget_s)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ranks.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg["dtype"], "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.config], "p": p, "buckets": nb, "bucket_mb": bucket_mb,
-                   "algo": args.algo, "sync": "in_place" if mode == D.DDP_SYNC_IN_PLACE else "flatten",
+                   "buffer_bytes": buf_bytes, "algo": args.algo,
+                   "sync": "in_place, one launch with the buffer broadcast" if one_launch else "flatten",
                    "divisor": divisor,
-                   "l2": l2_note(sum(a.numel() * a.element_size() for a in arenas), dev),
+                   "l2": l2_note(sum(a.numel() * a.element_size() for a in host_in), dev),
                    "parallelism": f"replicas only: {ranks.world} independent GPU(s)"},
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic,
-                     "algorithmic_bytes_per_launch": int(ab["allreduce"]) if launches_per_sync else None,
-                     "avg_launch_us": round(1e3 * statistics.mean(sync_ms), 2) if launches_per_sync else None,
-                     "avg_sync_us": round(1e3 * statistics.mean(sync_ms), 2),
-                     "event_timed_launches": len(sync_ms), "event_every_steps": EVENT_EVERY},
-        "allreduce_gbs": round(achieved, 1),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": int(kernel_bytes),
+                     "avg_launch_us": round(avg_us, 2), "event_timed_launches": roof_launches,
+                     "timing": "CUDA events around the launches, back to back on the launching stream"},
+        "allreduce_gbs": round(ab["allreduce"] / (avg_us / 1e6) / 1e9, 1),
         "buckets_per_s": round(nb * args.steps * ranks.world / (ms_max / 1e3), 1),
-        "busbw_gbs": round(sum(n * esz for n in red.bucket_numel) / (statistics.mean(sync_ms) / 1e3) / 1e9
-                           * 2 * (p - 1) / p, 1),
+        "busbw_gbs": round(sum(n * esz for n in red_bucket_numel(cfg)) / (avg_us / 1e6) / 1e9 * 2 * (p - 1) / p, 1),
+        "two_launch_form": two_launch,
         "flatten_form": other,
         "cuda_graph": graph,
+        **extras,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
     if ranks.rank == 0:
         print(json.dumps(line), flush=True)
 
 
+def red_bucket_numel(cfg):
+    """Elements of every bucket of the workload (the oracle's plan, which the
+    library's equals: checked by the tests)."""
+    from oracle import buckets as ob
+    from synth import workloads as W
+    numel = W.numels(cfg)
+    _, _, bnumel = ob.bucket_layout(numel, ob.assign_buckets(numel, W.esize(cfg), cfg["first_cap"], cfg["cap"]))
+    return bnumel
+
+
+def make_flush():
+    """An L2 flush: a 512 MiB write, then a 512 MiB read of another buffer, so
+    the next launch starts with clean lines that belong to neither."""
+    import torch
+    wflush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    rflush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
+
+    def flush():
+        wflush.fill_(1)
+        rflush.sum()
+    return flush
+
+
+def time_point(call, nsets, reps, batches, flush, graph=True):
+    """Batches of launches call(0), call(1), ... (call(i) uses input copy
+    i mod nsets), L2 flushed before each batch. Returns (seconds per launch:
+    graph-replayed if graph else eager, eager seconds per launch, launches per
+    batch, batches). A batch has up to `reps` launches, fewer when one launch
+    is long (about 5 ms of work per batch is enough)."""
+    import torch
+    for i in range(min(nsets, 3) + 1):
+        call(i)
+    flush()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    call(0)
+    b.record()
+    b.synchronize()
+    t1 = a.elapsed_time(b) / 1e3
+    nrep = max(3, min(reps, int(math.ceil(5e-3 / max(t1, 1e-9)))))
+    nbat = batches if t1 < 1e-3 else 3
+
+    def batch():
+        for i in range(nrep):
+            call(i)
+
+    def timed(run):
+        out = []
+        for _ in range(nbat):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run()
+            b.record()
+            b.synchronize()
+            out.append(a.elapsed_time(b) / 1e3 / nrep)
+        return statistics.median(out)
+
+    t_eager = timed(batch)
+    t_graph = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            batch()
+        g.replay()
+        torch.cuda.synchronize()
+        t_graph = timed(g.replay)
+        del g
+    return (t_graph if t_graph is not None else t_eager), t_eager, nrep, nbat
+
+
+def sweep_sets(p, n, with_outs, reps, out_elems=None):
+    """Input copies for one sweep point: enough copies that no launch of a
+    batch finds its inputs in L2 when one copy is under 2x L2 (at most 4 GiB
+    of copies), values uniform on [-1, 1)."""
+    import torch
+
+    import synth
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    out_elems = out_elems or n
+    set_bytes = p * n * 4 + (p * out_elems * 4 if with_outs else 0)
+    nsets = 1
+    if set_bytes < 2 * l2:
+        nsets = max(1, min(reps, (4 << 30) // set_bytes))
+    sets = []
+    for _ in range(nsets):
+        bufs = []
+        for r in range(p):
+            t = torch.empty(n, dtype=torch.float32, device="cuda")
+            synth.fill_(t, "uniform", 1005, r)
+            bufs.append(t)
+        outs = [torch.empty(out_elems, dtype=torch.float32, device="cuda") for _ in range(p)] if with_outs else []
+        sets.append((bufs, outs))
+    return sets
+
+
+def bench_sweep_points(peak, ps=(2, 8, 64), sizes_mib=(1, 25, 256), reps=20, batches=5):
+    """The metric's two axes for the bench line: the fused all-reduce of one
+    fp32 buffer of M MiB on each of p replicas, graph-replayed batches after an
+    L2 flush (as --sweep times them)."""
+    import torch
+
+    import ring_all_reduce_ddp_gb300 as D
+    flush = make_flush()
+    out = []
+    for p in ps:
+        for mib in sizes_mib:
+            M = mib << 20
+            n = M // 4
+            sets = sweep_sets(p, n, False, reps)
+            call = lambda i, sets=sets, n=n, p=p: D.ddp_allreduce(sets[i % len(sets)][0], n, D.DDP_FLOAT32,
+                                                                  float(p), D.DDP_ALGO_FUSED)
+            t, t_eager, nrep, nbat = time_point(call, len(sets), reps, batches, flush)
+            gbs = 2 * p * M / t / 1e9
+            out.append({"op": "allreduce", "algo": "fused", "p": p, "bytes": M, "us": round(t * 1e6, 2),
+                        "us_eager": round(t_eager * 1e6, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                        "input_copies": len(sets), "reps": nrep, "batches": nbat})
+            del sets
+            torch.cuda.empty_cache()
+    return {"timing": "CUDA graph of a batch of launches, L2 flushed before each batch, median of batches",
+            "points": out}
+
+
+def bench_config_points(peak, reps=20):
+    """The other model-shaped gradient sets of the metric: GPT-2 small (fp32,
+    token-count divisor) and Llama-1B (bf16, with its 64 per-forward buffers),
+    each as the one-launch step, back-to-back launches timed by events."""
+    import torch
+
+    from ring_all_reduce_ddp_gb300.reducer import Reducer
+    from synth import workloads as W
+    out = {}
+    for name in ("gpt2_small", "llama_1b"):
+        cfg = W.CONFIGS[name]
+        p = cfg["p"]
+        grads, arenas = W.make_grads(cfg)
+        red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+        buf_bytes = 0
+        if cfg.get("buffers"):
+            bufs = W.buffer_set(cfg)
+            buf_bytes = red.set_buffers(bufs, 0)
+        Dv = W.divisor(cfg)
+        nbytes = red.algorithmic_bytes()["allreduce"] + p * buf_bytes
+        for _ in range(3):
+            red.step(Dv)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_l = reps if name == "gpt2_small" else max(8, reps // 2)
+        a.record()
+        for _ in range(n_l):
+            red.step(Dv)
+        b.record()
+        torch.cuda.synchronize()
+        us = 1e3 * a.elapsed_time(b) / n_l
+        gbs = nbytes / (us / 1e6) / 1e9
+        out[name] = {"workload": WORKLOAD_TEXT[name], "p": p, "dtype": cfg["dtype"], "buckets": len(red.buckets),
+                     "algorithmic_bytes": int(nbytes), "us": round(us, 2), "gbs": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "buckets_per_s": round(len(red.buckets) / (us / 1e6), 1),
+                     "launches": n_l}
+        red.destroy()
+        del red, grads, arenas
+        torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------- reference arm
 def run_reference(args, ranks: Ranks):
-    """The CPU oracle as it stands, on rank 0 only. Each step runs the oracle's
-    literal ring all-reduce on all p replicas of a leading slice of the
-    workload's first bucket, the slice sized so the whole run takes under a
-    minute (the whole bucket when steps are few). Inputs are generated once,
-    outside the timed region."""
+    """The CPU oracle as it stands, on rank 0 only, on the GPU arm's step:
+    bucket assignment, the coalesced broadcast of the buffers, flatten +
+    literal ring all-reduce + unflatten of every bucket, all replicas, every
+    element. If --steps + --warmup whole steps would take more than about
+    two minutes, every step is the same sample of it instead: each bucket's
+    all-reduce on its leading fraction of elements (same_config is then
+    false). Inputs are generated once, outside the timed region."""
     if ranks.rank != 0:
         return
-    import numpy as np
-
-    from oracle import buckets as ob
-    from oracle import ring as orc
     from synth import workloads as W
     cfg = W.CONFIGS[args.config]
-    p, es = cfg["p"], W.esize(cfg)
-    numel = W.numels(cfg)
-    starts = W.tensor_starts(cfg)
-    plan = ob.assign_buckets(numel, es, cfg["first_cap"], cfg["cap"])
-    _, offset, bnumel = ob.bucket_layout(numel, plan)
-    n = bnumel[0]
-    members = plan[0]
-    flat = []
-    for r in range(p):
-        hv = {t: W.host_values(cfg, r, np.arange(starts[t], starts[t] + numel[t])) for t in members}
-        zero = np.zeros(0, np.float32 if es == 4 else np.uint16)
-        flat.append(ob.flatten([hv.get(t, zero) for t in range(len(numel))], members, offset, n))
-    Dv = W.divisor(cfg)
+    p = cfg["p"]
+    grads, bufs = oracle_inputs(cfg)
     t0 = time.perf_counter()
-    orc.allreduce(flat, n, Dv, cfg["dtype"])
+    oracle_step(cfg, grads, bufs)  # one whole step, untimed, sizes the run
     t_full = time.perf_counter() - t0
-    budget = 45.0
+    budget = 120.0
     frac = min(1.0, budget / max(1e-9, (args.steps + args.warmup) * t_full))
-    m = max(64 * p, int(n * frac))
-    sample = [f[:m].copy() for f in flat]  # the first m elements of the bucket, reduced as one buffer
     for _ in range(max(args.warmup, 0)):
-        orc.allreduce(sample, m, Dv, cfg["dtype"])
+        oracle_step(cfg, grads, bufs, frac)
     t_tot = 0.0
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        orc.allreduce(sample, m, Dv, cfg["dtype"])
+        oracle_step(cfg, grads, bufs, frac)
         t_tot += time.perf_counter() - t0
-    nbytes = 2 * p * m * es * args.steps
+    nbytes = oracle_step_bytes(cfg, frac) * args.steps
     value = nbytes / t_tot / 1e9
-    desc = (f"oracle literal ring all-reduce, per step, of the first {m} of the {n} elements of bucket 0 "
-            f"(p={p}), single thread")
+    ms_step = 1e3 * t_tot / max(args.steps, 1)
+    if frac >= 1:
+        desc = (f"the whole step in the oracle every step: bucket assignment, coalesced broadcast of the buffers, "
+                f"flatten + literal ring all-reduce + unflatten of every bucket (p={p}, every element); "
+                f"single thread; bytes counted as the GPU arm counts them (2pM + pB)")
+    else:
+        desc = (f"a sample of the step in the oracle every step: the buffers' broadcast and each bucket's literal "
+                f"ring all-reduce on its leading {frac:.4f} of elements (p={p}); single thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ranks.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_tot / max(args.steps, 1), 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg["dtype"],
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.config], "p": p, "algo": "oracle literal ring"},
+        "config": {"workload": WORKLOAD_TEXT[args.config], "p": p, "algo": "oracle literal ring",
+                   "same_config": frac >= 1, "sample_fraction": round(frac, 6)},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle", "cores": 1, "sample": desc,
-                         "host_cores_available": cores_used(), "cpu_model": cpu_model()},
+                         "ms_per_step": round(ms_step, 3), "host_cores_available": cores_used(),
+                         "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
 
 # --------------------------------------------------------------- sweep
 def literal_traffic_bytes(op: str, algo: str, p: int, M: int):
@@ -625,7 +866,6 @@ def run_sweep(args, ranks: Ranks):
 
     import ring_all_reduce_ddp_gb300 as D
     from ring_all_reduce_ddp_gb300 import build as B
-    import synth
     B.build_library()
     if ranks.rank != 0:
         return
@@ -639,14 +879,7 @@ def run_sweep(args, ranks: Ranks):
     tree_codes = {"rd": D.DDP_ALGO_RECURSIVE_DOUBLING, "rab": D.DDP_ALGO_RABENSEIFNER, "tree": D.DDP_ALGO_TREE}
     reps = int(os.environ.get("SWEEP_REPS", "20"))
     batches = int(os.environ.get("SWEEP_BATCHES", "5"))
-    wflush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
-    rflush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    rotate_budget = 4 << 30
-
-    def flush():
-        wflush.fill_(1)
-        rflush.sum()
+    flush = make_flush()
 
     for p in ps:
         for k in range(min_k, max_k + 1):
@@ -656,21 +889,8 @@ def run_sweep(args, ranks: Ranks):
             n = M // 4
             m = n // p
             with_outs = ops != "allreduce"
-            out_elems = max(n, p * m)
-            set_bytes = p * M + (p * out_elems * 4 if with_outs else 0)
-            nsets = 1
-            if set_bytes < 2 * l2:
-                nsets = max(1, min(reps, rotate_budget // set_bytes))
-            sets = []
-            for _ in range(nsets):
-                bufs = []
-                for r in range(p):
-                    t = torch.empty(n, dtype=torch.float32, device="cuda")
-                    synth.fill_(t, "uniform", 1005, r)
-                    bufs.append(t)
-                outs = [torch.empty(out_elems, dtype=torch.float32, device="cuda") for _ in range(p)] \
-                    if with_outs else []
-                sets.append((bufs, outs))
+            sets = sweep_sets(p, n, with_outs, reps, max(n, p * m))
+            nsets = len(sets)
             for op in ops.split(","):
                 for an in algos:
                     if an in ("persistent", "rd", "rab", "tree") and op != "allreduce":
@@ -693,49 +913,10 @@ def run_sweep(args, ranks: Ranks):
 
                     nbytes = {"allreduce": 2 * p * M, "allgather": M + p * M, "broadcast": p * M}.get(
                         op, p * M + M)
-
-                    # warm-up (first-use lookups, workspace pools), then one timed
-                    # launch to size the batch: up to `reps` launches, fewer when
-                    # one launch is long (a batch of about 5 ms is enough there)
-                    for i in range(min(nsets, 3) + 1):
-                        call(i)
-                    flush()
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record()
-                    call(0)
-                    b.record()
-                    b.synchronize()
-                    t1 = a.elapsed_time(b) / 1e3
-                    nrep = max(3, min(reps, int(math.ceil(5e-3 / max(t1, 1e-9)))))
-                    nbat = batches if t1 < 1e-3 else 3
-
-                    def batch(nrep=nrep):
-                        for i in range(nrep):
-                            call(i)
-
-                    def timed(run, nrep=nrep, nbat=nbat):
-                        out = []
-                        for _ in range(nbat):
-                            flush()
-                            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                            a.record()
-                            run()
-                            b.record()
-                            b.synchronize()
-                            out.append(a.elapsed_time(b) / 1e3 / nrep)
-                        return statistics.median(out)
-
-                    t_eager = timed(batch)
-                    t_graph = None
-                    if an != "persistent":
-                        g = torch.cuda.CUDAGraph()
-                        with torch.cuda.graph(g):
-                            batch()
-                        g.replay()
-                        torch.cuda.synchronize()
-                        t_graph = timed(g.replay)
-                        del g
-                    t = t_graph if t_graph is not None else t_eager
+                    # the persistent ring (a cooperative launch) is timed eagerly only
+                    t, t_eager, nrep, nbat = time_point(call, nsets, reps, batches, flush,
+                                                        graph=(an != "persistent"))
+                    t_graph = t if an != "persistent" else None
                     gbs = nbytes / t / 1e9
                     moved = literal_traffic_bytes(op, an, p, M)
                     line = {"sweep": op, "algo": an, "p": p, "bytes": M, "us": round(t * 1e6, 2),
@@ -752,16 +933,21 @@ def run_sweep(args, ranks: Ranks):
 
 # --------------------------------------------------------------- overlap
 def run_overlap(args, ranks: Ranks):
-    """Exposed communication against bucket cap, with readiness-driven firing.
+    """Exposed communication against bucket cap and the comm kernels' grid,
+    with readiness-driven firing.
 
     A synthetic backward walks the parameters last-registered first on the
     compute stream; each weight gradient costs two bf16 GEMMs with
     4 * numel * n_tok FLOPs in all (backward is about 4N FLOPs per token);
     after each gradient an event is recorded and the Reducer is told the
     gradient is ready, which launches every newly complete bucket's in-place
-    all-reduce on a communication stream. For each cap: the backward alone,
-    backward + overlapped sync, and backward followed by the sync. One JSON
-    line per cap."""
+    all-reduce on a communication stream. A step ends when the compute stream
+    has waited for the communication stream (the optimizer needs the reduced
+    gradients). For each cap, comm-stream priority and grid cap of the bucket
+    launches (0: one block per 4 KB tile; N > 0: N blocks striding over the
+    tiles, so the all-reduces hold at most about N/6 SMs): the backward alone,
+    backward + overlapped sync (with the time the compute stream took inside
+    it), and backward followed by the sync. One JSON line per point."""
     import torch
 
     import ring_all_reduce_ddp_gb300 as D
@@ -789,11 +975,10 @@ def run_overlap(args, ranks: Ranks):
     # backward's GEMM blocks)
     lo_prio, hi_prio = torch.cuda.Stream.priority_range()
     comm_streams = {"normal": torch.cuda.Stream(priority=lo_prio), "high": torch.cuda.Stream(priority=hi_prio)}
-    comm = comm_streams["normal"]
 
     ready_events = [torch.cuda.Event() for _ in range(k)]
 
-    def backward(red=None):
+    def backward(red=None, comm=None):
         for t in range(k - 1, -1, -1):
             cols = (numel[t] + kdim - 1) // kdim
             if numel[t] >= 4096:  # 2 GEMMs: 2 * (2 * n_tok * kdim * cols) ~ 4 * numel * n_tok FLOPs
@@ -803,48 +988,69 @@ def run_overlap(args, ranks: Ranks):
                 ready_events[t].record(compute)
                 red.mark_ready(t, divisor, ready_events[t], comm)
 
-    def timed(fn, reps):
+    def timed(fn, reps, comm=None):
+        """Mean per step of (compute-stream time, time until both streams are done)."""
+        def one():
+            fn()
+            c = torch.cuda.Event(enable_timing=True)
+            c.record(compute)
+            if comm is not None:
+                compute.wait_stream(comm)
+            return c
         for _ in range(3):
-            fn()
+            one()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(compute)
+        ev = []
         for _ in range(reps):
-            fn()
-        for cs in comm_streams.values():
-            compute.wait_stream(cs)
-        b.record(compute)
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(compute)
+            c = one()
+            s1.record(compute)
+            ev.append((s0, c, s1))
         torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
+        return (statistics.mean(a.elapsed_time(c) for a, c, _ in ev),
+                statistics.mean(a.elapsed_time(b) for a, _, b in ev))
 
-    reps = max(5, min(args.steps, 50))
-    t_bwd = timed(lambda: backward(None), reps)
+    reps = max(5, min(args.steps, 20))
+    _, t_bwd = timed(lambda: backward(None), reps)
     flops = 4.0 * sum(n for n in numel if n >= 4096) * n_tok
-    caps = [int(float(c) * (1 << 20)) for c in os.environ.get("OVERLAP_CAPS_MB", "0.25,1,5,25,100,100000").split(",")]
+    caps = [int(float(c) * (1 << 20)) for c in os.environ.get("OVERLAP_CAPS_MB", "1,5,25").split(",")]
     prios = os.environ.get("OVERLAP_PRIORITIES", "normal,high").split(",")
-    for cap, prio in [(c, q) for c in caps for q in prios]:
-        comm = comm_streams[prio]
+    blocks = [int(b) for b in os.environ.get("OVERLAP_COMM_BLOCKS", "0,24,48,96,192,384").split(",")]
+    for cap in caps:
         red = Reducer(grads, min(cfg["first_cap"], cap), cap)
-
-        def overlapped():
-            red.prepare()
-            backward(red)
+        _, t_comm = timed(lambda: red.sync_gradients(divisor, D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE, 1.0, compute),
+                          reps)
 
         def serial():
             backward(None)
             red.sync_gradients(divisor, D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE, 1.0, compute)
 
-        t_ov = timed(overlapped, reps)
-        t_se = timed(serial, reps)
-        t_comm = timed(lambda: red.sync_gradients(divisor, D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE, 1.0, compute), reps)
-        print(json.dumps({"overlap": args.config, "p": cfg["p"], "bucket_cap_mb": cap / (1 << 20),
-                          "comm_stream_priority": prio,
-                          "buckets": len(red.buckets), "n_tok": n_tok,
-                          "backward_ms": round(t_bwd, 4), "backward_tflops": round(flops / (t_bwd / 1e3) / 1e12, 1),
-                          "sync_alone_ms": round(t_comm, 4), "overlapped_ms": round(t_ov, 4),
-                          "serial_ms": round(t_se, 4), "exposed_ms": round(t_ov - t_bwd, 4),
-                          "hidden_frac": (round(1 - (t_ov - t_bwd) / (t_se - t_bwd), 3)
-                                          if t_se - t_bwd > 0.05 * t_comm else None)}), flush=True)
+        _, t_se = timed(serial, reps)
+        for prio in prios:
+            comm = comm_streams[prio]
+            for nblk in blocks:
+                red.set_comm_blocks(nblk)
+
+                def overlapped():
+                    red.prepare()
+                    backward(red, comm)
+
+                t_cmp, t_ov = timed(overlapped, reps, comm)
+                exposed = t_ov - t_bwd
+                print(json.dumps({"overlap": args.config, "p": cfg["p"], "bucket_cap_mb": cap / (1 << 20),
+                                  "comm_stream_priority": prio, "comm_blocks": nblk,
+                                  "comm_sm_equivalent": round(nblk / 6, 1) if nblk else None,
+                                  "buckets": len(red.buckets), "n_tok": n_tok,
+                                  "backward_ms": round(t_bwd, 4),
+                                  "backward_tflops": round(flops / (t_bwd / 1e3) / 1e12, 1),
+                                  "sync_alone_ms": round(t_comm, 4), "serial_ms": round(t_se, 4),
+                                  "overlapped_ms": round(t_ov, 4), "backward_in_overlap_ms": round(t_cmp, 4),
+                                  "gemm_slowdown_ms": round(t_cmp - t_bwd, 4), "tail_ms": round(t_ov - t_cmp, 4),
+                                  "exposed_ms": round(exposed, 4),
+                                  "hidden_frac": round(1 - exposed / (t_se - t_bwd), 3) if t_se > t_bwd else None}),
+                      flush=True)
+        red.set_comm_blocks(0)
         red.destroy()
 
 

@@ -16,7 +16,8 @@
  *   - The caller owns every replica, input and output buffer. The library
  *     allocates only:
  *       a handle's device memory, freed by its destroy call: a ddp_ring's
- *       workspace; a ddp_reducer's flat buckets, piece table and workspace;
+ *       workspace; a ddp_reducer's flat buckets, piece table, buffer table and
+ *       workspace;
  *       stream-ordered temporaries (cudaMallocAsync / cudaFreeAsync on the
  *       caller's stream) for the literal schedules of one-shot calls, the
  *       persistent ring's step flags, and the fp32 workspace of the bf16
@@ -26,6 +27,7 @@
  *     host, as DDP's per-bucket futures do ([DDP] Part 2, "Step 3:
  *     finalize_backward"). Only these wait for the device: ddp_ring_sync,
  *     ddp_device_error, ddp_reducer_create (its piece-table upload),
+ *     ddp_reducer_set_buffers (its table upload),
  *     ddp_reducer_rebuild (drains the device first), the destroy calls, and
  *     every collective while the call log (DDP_RING_LOG) is on.
  *   - Threads: calls on different handles, or handle-free calls, may run
@@ -46,7 +48,8 @@
  *   - Call log: with the environment variable DDP_RING_LOG=<path> set when
  *     the library first logs, each collective call (ddp_allreduce, _ex,
  *     _persistent, ddp_reduce_scatter, ddp_allgather, ddp_broadcast,
- *     _coalesced, ddp_bucket_allreduce, ddp_reducer_sync) appends one JSON
+ *     _coalesced, ddp_bucket_allreduce, ddp_reducer_sync, ddp_reducer_step)
+ *     appends one JSON
  *     line to <path>: op, algo, p, n, dtype, bytes_algorithmic (inputs read
  *     once, outputs written once), bytes_per_rank (what one simulated rank
  *     sends in the method's schedule, the pages' per-rank byte counter),
@@ -343,6 +346,39 @@ ddp_status ddp_reducer_sync(ddp_reducer* handle, float divisor, float predivide,
                             ddp_sync_mode mode, cudaStream_t stream);
 ddp_status ddp_reducer_destroy(ddp_reducer* handle);
 
+/* The per-forward buffer broadcast and the gradient sync in ONE launch.
+ * [DDP] Part 2: every forward starts with _sync_buffers, a
+ * _broadcast_coalesced of the module's buffers from rank 0 (the annotated
+ * trace), and every backward ends with the Reducer's bucket all-reduces
+ * (mark_variable_ready / finalize_backward).
+ * ddp_reducer_set_buffers attaches k buffers to the reducer:
+ *   tensors[p*k]: tensors[r*k + j] is replica r's buffer j (device pointers,
+ *   kept, not copied, until the next set_buffers or destroy), nbytes[k] bytes
+ *   each, root: the replica whose buffers are copied to the others. The copy
+ *   is bitwise, whatever the buffers' own dtypes, but each buffer's bytes must
+ *   be a multiple of the gradients' element size (DDP_ERR_ARG) and every
+ *   pointer aligned to it (DDP_ERR_ALIGN). Buffers must not overlap one
+ *   another or any gradient of the reducer (DDP_ERR_ARG). The buffers join the
+ *   reducer's piece table, which is rebuilt in device memory: the call waits
+ *   for the device. If that allocation fails (DDP_ERR_NOMEM), no buffers stay
+ *   attached and the reducer refuses sync, step, prepare and mark_ready
+ *   (DDP_ERR_STATE) until a ddp_reducer_rebuild succeeds. k == 0 detaches.
+ *   The buffers stay attached across ddp_reducer_rebuild.
+ * ddp_reducer_step enqueues on `stream` one launch that does both: the
+ *   attached buffers copied from root to every other replica (the bits of
+ *   ddp_broadcast_coalesced; the root's buffers are read, not written) and
+ *   every bucket's in-place sync with `divisor` (the bits of
+ *   ddp_reducer_sync with DDP_SYNC_IN_PLACE, which never touches the
+ *   buffers). The two touch disjoint memory, so the result equals the two
+ *   calls in either order. In a training loop it is the sync at the end of
+ *   backward together with the buffer broadcast that the next forward needs
+ *   (nothing between the two reads or writes the buffers). With no buffers
+ *   attached it is ddp_reducer_sync(DDP_SYNC_IN_PLACE). Same errors as
+ *   ddp_reducer_sync. */
+ddp_status ddp_reducer_set_buffers(ddp_reducer* handle, int32_t k, void* const* tensors,
+                                   const int64_t* nbytes, int32_t root);
+ddp_status ddp_reducer_step(ddp_reducer* handle, float divisor, cudaStream_t stream);
+
 /* Readiness-driven firing, as the Reducer's hooks do it during backward
  * ([DDP] Part 2 "Step 2: backward": mark_variable_ready decrements the
  * bucket's pending count; mark_bucket_ready reduces every contiguous complete
@@ -369,6 +405,15 @@ ddp_status ddp_reducer_destroy(ddp_reducer* handle);
  *   ddp_reducer_sync, _prepare and _mark_ready then return DDP_ERR_STATE
  *   until a rebuild succeeds; destroy works as always. */
 ddp_status ddp_reducer_prepare(ddp_reducer* handle);
+/* The grid of the bucket launches ddp_reducer_mark_ready fires: max_blocks
+ * == 0 (the default) gives one block per 4 KB tile; max_blocks > 0 at most
+ * that many blocks, each striding over the bucket's tiles, as a collective
+ * library bounds its kernels to a few channels. A bounded grid holds at most
+ * max_blocks / (blocks resident per SM) SMs, so a backward pass running on
+ * another stream keeps the others ([DP] "Overlapping communication with the
+ * backward pass"). Results are the same bits for every value.
+ * DDP_ERR_ARG if max_blocks < 0. */
+ddp_status ddp_reducer_set_comm_blocks(ddp_reducer* handle, int32_t max_blocks);
 ddp_status ddp_reducer_mark_ready(ddp_reducer* handle, int32_t tensor, float divisor, cudaEvent_t ready,
                                   cudaStream_t comm_stream, int32_t* fired);
 int32_t ddp_reducer_observed(const ddp_reducer* handle, int32_t* order);
@@ -392,8 +437,13 @@ ddp_status ddp_reducer_rebuild(ddp_reducer* handle, const int32_t* order);
  *   GPU (different streams, or threads) race on it: order them on one stream.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture. Every GPU that loads the library holds the
- *   8 MiB until the process exits. */
+ *   before any stream capture. The address is kept for as long as the
+ *   device's context lives: after a cudaDeviceReset the next call looks it
+ *   up again in the new context (so that call, too, should come before any
+ *   capture). Every GPU that loads the library holds the 8 MiB until the
+ *   process exits.
+ *   n == 0 returns DDP_OK without reading the pointers, as ddp_reduce_scatter
+ *   does. */
 ddp_status ddp_reduce_scatter_noalloc(const void* const* in, void* const* out, int32_t p, int64_t n,
                                       ddp_dtype dtype, float divisor, ddp_own own, cudaStream_t stream);
 

@@ -59,6 +59,9 @@ _SIGS = {
     "ddp_reducer_bucket": [_c_vp, _c_i32, _P_i64, _P_vp],
     "ddp_reducer_sync": [_c_vp, _c_f32, _c_f32, _c_i32, _c_i32, _c_vp],
     "ddp_reducer_destroy": [_c_vp],
+    "ddp_reducer_set_buffers": [_c_vp, _c_i32, _P_vp, _P_i64, _c_i32],
+    "ddp_reducer_step": [_c_vp, _c_f32, _c_vp],
+    "ddp_reducer_set_comm_blocks": [_c_vp, _c_i32],
     "ddp_reducer_prepare": [_c_vp],
     "ddp_reducer_mark_ready": [_c_vp, _c_i32, _c_f32, _c_vp, _c_vp, _P_i32],
     "ddp_reducer_observed": [_c_vp, _P_i32],
@@ -343,6 +346,25 @@ class DDPReducer:
              predivide: float = 1.0, stream=None):
         _check(lib().ddp_reducer_sync(self.h, float(divisor), float(predivide), int(algo), int(mode),
                                       _stream(stream)))
+
+    def set_buffers(self, buffers, root: int = 0):
+        """Attach the per-forward buffers (p lists of k tensors, replica-major)
+        that ddp_reducer_step broadcasts from `root`; an empty list detaches."""
+        k = len(buffers[0]) if buffers else 0
+        if buffers and len(buffers) != self.p:
+            raise ValueError(f"need buffers for {self.p} replicas, got {len(buffers)}")
+        nbytes = [t.numel() * t.element_size() for t in buffers[0]] if k else []
+        self._bufs = _ptrs([t for row in buffers for t in row]) if k else None
+        _check(lib().ddp_reducer_set_buffers(self.h, k, self._bufs, _i64s(nbytes), int(root)))
+        return sum(nbytes)
+
+    def step(self, divisor: float, stream=None):
+        """The attached buffers' broadcast and the in-place sync, one launch."""
+        _check(lib().ddp_reducer_step(self.h, float(divisor), _stream(stream)))
+
+    def set_comm_blocks(self, max_blocks: int):
+        """Grid cap of the bucket launches mark_ready fires (0: one block per tile)."""
+        _check(lib().ddp_reducer_set_comm_blocks(self.h, int(max_blocks)))
 
     def prepare(self):
         _check(lib().ddp_reducer_prepare(self.h))

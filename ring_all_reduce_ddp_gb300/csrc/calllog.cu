@@ -242,4 +242,24 @@ ddp_status ddp_reducer_sync(ddp_reducer* h, float divisor, float predivide, ddp_
   return st;
 }
 
+ddp_status ddp_reducer_step(ddp_reducer* h, float divisor, cudaStream_t stream) {
+  CallTimer t(stream);
+  const ddp_status st = reducer_step_impl(h, divisor, stream);
+  int32_t p = 0;
+  ddp_dtype dt = DDP_FLOAT32;
+  std::vector<int64_t> bn;
+  reducer_shape(h, &p, &dt, &bn);
+  int64_t n = 0, rank_bytes = 0;
+  for (int64_t nb : bn) {
+    n += nb;
+    rank_bytes += allreduce_rank_bytes(DDP_ALGO_FUSED, p, nb, esize(dt));
+  }
+  const int64_t buf = reducer_buffer_bytes(h);
+  // the sync reads and writes every replica once (2pM); the broadcast reads the
+  // root's buffers once and writes the p - 1 others (p B)
+  log_call(t, "ddp_reducer_step", DDP_ALGO_FUSED, p, n, dt, 2 * static_cast<int64_t>(p) * n * esize(dt) + p * buf,
+           rank_bytes + static_cast<int64_t>(ceil_log2(p)) * buf, st);
+  return st;
+}
+
 }  // extern "C"

@@ -316,10 +316,11 @@ ddp_status plan_bucket_launches(int32_t p, int32_t k, const void* const* grads, 
   return DDP_OK;
 }
 
-ddp_status run_bucket_launches(std::vector<BucketArgs>& launches, ddp_dtype dt, float divisor, cudaStream_t s) {
+ddp_status run_bucket_launches(std::vector<BucketArgs>& launches, ddp_dtype dt, float divisor, cudaStream_t s,
+                                int32_t max_blocks) {
   for (BucketArgs& a : launches) {
     a.divisor = divisor;
-    DDP_CUDA(launch_bucket_allreduce(a, dt, s), "bucket all-reduce launch");
+    DDP_CUDA(launch_bucket_allreduce(a, dt, s, max_blocks), "bucket all-reduce launch");
   }
   return DDP_OK;
 }

@@ -81,7 +81,8 @@ ddp_status check_bucket_layout(int32_t p, int32_t k, const void* const* grads, c
 ddp_status plan_bucket_launches(int32_t p, int32_t k, const void* const* grads, const int64_t* numel,
                                 const int64_t* offset, ddp_dtype dt, float divisor,
                                 std::vector<BucketArgs>& out);
-ddp_status run_bucket_launches(std::vector<BucketArgs>& launches, ddp_dtype dt, float divisor, cudaStream_t s);
+ddp_status run_bucket_launches(std::vector<BucketArgs>& launches, ddp_dtype dt, float divisor, cudaStream_t s,
+                                int32_t max_blocks = 0);
 void write_assignment(const std::vector<std::vector<int32_t>>& buckets, const int64_t* numel, int32_t* n_buckets,
                       int32_t* bucket_of, int64_t* offset, int32_t* bucket_ptr, int32_t* bucket_tensors,
                       int64_t* bucket_numel);
@@ -291,6 +292,9 @@ ddp_status bucket_allreduce_impl(int32_t p, int32_t k, void* const* grads, const
                                  const int64_t* offset, ddp_dtype dtype, float divisor, cudaStream_t stream);
 ddp_status reducer_sync_impl(ddp_reducer* h, float divisor, float predivide, ddp_algo algo, ddp_sync_mode mode,
                              cudaStream_t stream);
+ddp_status reducer_step_impl(ddp_reducer* h, float divisor, cudaStream_t stream);
+// Bytes of one replica's buffers attached for ddp_reducer_step (0 if none).
+int64_t reducer_buffer_bytes(const ddp_reducer* h);
 // A reducer's replica count, dtype and bucket sizes (elements), for the log.
 void reducer_shape(const ddp_reducer* h, int32_t* p, ddp_dtype* dt, std::vector<int64_t>* bucket_numel);
 

@@ -12,6 +12,8 @@
 // same bits as the ring on the flat bucket. Work is cut into pieces (a tensor
 // intersected with a chunk: one origin each) and pieces into tiles of
 // bucket_tile_elems elements per replica; one block per tile.
+#include <algorithm>
+
 #include "launch.h"
 
 namespace ddp {
@@ -71,7 +73,13 @@ __device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divi
   const int64_t len = min(kTile, a.start[i] + a.len[i] - t0);
   if (len <= 0) return;
   void* const* rep = a.ptr + static_cast<int64_t>(a.slot[i]) * p;
-  const int o = a.origin[i];
+  // origin >= p marks a copy piece, one of the per-forward buffers that the
+  // Reducer's one-launch step broadcasts ("PyTorch DDP Deep Dive", Part 2,
+  // _sync_buffers -> _broadcast_coalesced): replica origin - p's bits are
+  // written to every other replica, nothing is summed, the root is not written.
+  const int oi = a.origin[i];
+  const bool copy = oi >= p;
+  const int o = copy ? oi - p : oi;
 
   // The replicas in ring order o, o+1, ... (mod p), staged in shared memory
   // rather than held in registers: 40 registers instead of 74 at p = 8, so six
@@ -98,6 +106,22 @@ __device__ __forceinline__ void bucket_tile(const View& a, int32_t b, float divi
   if (same) head = min(static_cast<int64_t>(((16u - (a0 & 15u)) & 15u) / sizeof(T)), len);
   const int64_t nvec = (len - head) / V;
   const int64_t tail0 = head + nvec * V;
+
+  if (copy) {
+    for (int64_t e = threadIdx.x; e < head + (len - tail0); e += blockDim.x) {
+      const int64_t x = t0 + (e < head ? e : tail0 + (e - head));
+      const T y = reinterpret_cast<const T*>(rep[o])[x];
+      for (int q = 0; q < p; ++q)
+        if (q != o) reinterpret_cast<T*>(rep[q])[x] = y;
+    }
+    for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x) {
+      const int64_t x = t0 + head + v * V;
+      const uint4 y = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(rep[o]) + x);
+      for (int q = 0; q < p; ++q)
+        if (q != o) *reinterpret_cast<uint4*>(reinterpret_cast<T*>(rep[q]) + x) = y;
+    }
+    return;
+  }
 
   for (int64_t e = threadIdx.x; e < head + (len - tail0); e += blockDim.x) {
     const int64_t x = t0 + (e < head ? e : tail0 + (e - head));
@@ -180,8 +204,9 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce_table(const Bucke
 // kernel in the stream (usually the previous bucket's), so its blocks start
 // while that kernel's last wave drains.
 template <typename T>
-cudaError_t by_value(const BucketArgs& a, cudaStream_t s) {
-  const dim3 grid(a.tile0[a.npieces]), block(kThreads);
+cudaError_t by_value(const BucketArgs& a, cudaStream_t s, int32_t max_blocks) {
+  const int32_t tiles = a.tile0[a.npieces];
+  const dim3 grid(max_blocks > 0 ? std::min(tiles, max_blocks) : tiles), block(kThreads);
   cudaError_t e;
   switch (a.p) {
     case 2: e = launch_pdl(k_bucket_allreduce<T, 2>, grid, block, 0, s, a); break;
@@ -230,9 +255,9 @@ cudaError_t by_table(const BucketTable& t, int32_t tiles, float divisor, cudaStr
 
 }  // namespace
 
-cudaError_t launch_bucket_allreduce(const BucketArgs& a, ddp_dtype dt, cudaStream_t s) {
+cudaError_t launch_bucket_allreduce(const BucketArgs& a, ddp_dtype dt, cudaStream_t s, int32_t max_blocks) {
   if (a.npieces <= 0 || a.tile0[a.npieces] <= 0) return cudaSuccess;
-  return dt == DDP_FLOAT32 ? by_value<float>(a, s) : by_value<__nv_bfloat16>(a, s);
+  return dt == DDP_FLOAT32 ? by_value<float>(a, s, max_blocks) : by_value<__nv_bfloat16>(a, s, max_blocks);
 }
 
 cudaError_t launch_bucket_table(const BucketTable& t, int32_t total_tiles, float divisor, ddp_dtype dt,

@@ -13,7 +13,8 @@ int64_t launches();
 cudaError_t launch_fused_reduce(const FusedArgs& a, ddp_dtype dt, bool staged, cudaStream_t s);
 cudaError_t launch_rs_step_inplace_f32(const RingStepArgs& a, cudaStream_t s);
 cudaError_t launch_rs_step_ws(const RingStepArgs& a, ddp_dtype dt, cudaStream_t s);
-cudaError_t launch_bucket_allreduce(const BucketArgs& a, ddp_dtype dt, cudaStream_t s);
+// max_blocks > 0 caps the grid: each block then strides over the tiles.
+cudaError_t launch_bucket_allreduce(const BucketArgs& a, ddp_dtype dt, cudaStream_t s, int32_t max_blocks = 0);
 cudaError_t launch_bucket_table(const BucketTable& t, int32_t total_tiles, float divisor, ddp_dtype dt,
                                 cudaStream_t s);
 cudaError_t launch_ring_persistent(const PersistArgs& a, cudaStream_t s);

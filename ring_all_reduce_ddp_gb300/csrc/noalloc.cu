@@ -22,22 +22,59 @@ namespace {
 constexpr int64_t kNoAllocScratchBytes = int64_t(8) << 20;  // 8 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[64] = {nullptr};
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;  // the context the address belongs to (0: none looked up yet)
+  void* ptr = nullptr;
+};
+ScratchAddr g_noalloc_addr[64];
 
-// The array's device address on the current device, looked up once per device.
-// In host code the array's name is only a stand-in: the address a kernel may
-// use is the one cudaGetSymbolAddress returns with that device current.
+// The driver's cuCtxGetId, reached through the runtime (the library does not
+// link the driver library itself). It returns an id that no other context of
+// the process ever gets, so a destroyed and re-created primary context
+// (cudaDeviceReset) is told apart from the one an address was looked up in.
+using CtxGetIdFn = int (*)(void* ctx, unsigned long long* id);
+
+ddp_status current_context_id(unsigned long long* id) {
+  static CtxGetIdFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    (void)cudaGetLastError();
+    return reinterpret_cast<CtxGetIdFn>(f);
+  }();
+  DDP_CHECK(fn != nullptr, DDP_ERR_CUDA, "the driver has no cuCtxGetId");
+  if (fn(nullptr, id) != 0) {
+    // No context current on this thread yet: cudaSetDevice binds the current
+    // device's primary context (and allocates nothing on it).
+    int dev = 0;
+    DDP_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    DDP_CUDA(cudaSetDevice(dev), "cudaSetDevice");
+    DDP_CHECK(fn(nullptr, id) == 0, DDP_ERR_CUDA, "cuCtxGetId of the current context failed");
+  }
+  return DDP_OK;
+}
+
+// The array's device address in the current device's context, looked up once
+// per device and context. In host code the array's name is only a stand-in:
+// the address a kernel may use is the one cudaGetSymbolAddress returns with
+// that device current, and it lasts as long as the context does.
 ddp_status noalloc_scratch(float** out) {
   int dev = 0;
   DDP_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
   DDP_CHECK(dev >= 0 && dev < 64, DDP_ERR_ARG, "device index out of range");
+  unsigned long long ctx = 0;
+  DDP_TRY(current_context_id(&ctx));
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  ScratchAddr& a = g_noalloc_addr[dev];
+  if (a.ptr == nullptr || a.ctx_id != ctx) {
     void* ptr = nullptr;
     DDP_CUDA(cudaGetSymbolAddress(&ptr, g_noalloc_scratch), "cudaGetSymbolAddress of the scratch array");
-    g_noalloc_ptr[dev] = ptr;
+    a.ptr = ptr;
+    a.ctx_id = ctx;
   }
-  *out = static_cast<float*>(g_noalloc_ptr[dev]);
+  *out = static_cast<float*>(a.ptr);
   return DDP_OK;
 }
 
@@ -60,6 +97,7 @@ extern "C" ddp_status ddp_reduce_scatter_noalloc(const void* const* in, void* co
   DDP_TRY(check_common(p, n, dtype));
   DDP_TRY(check_divisor(divisor));
   DDP_TRY(check_own(own));
+  if (n == 0) return DDP_OK;  // a no-op whatever the pointers, as in ddp_reduce_scatter
   DDP_TRY(check_ptrs(in, p, "in"));
   DDP_TRY(check_ptrs(const_cast<const void* const*>(out), p, "out"));
   if (own == DDP_OWN_RANK)
@@ -81,7 +119,6 @@ extern "C" ddp_status ddp_reduce_scatter_noalloc(const void* const* in, void* co
     all[p] = range_of(in[r], n * es);
     DDP_CHECK(disjoint_inplace(all, p + 1), DDP_ERR_ARG, "an output buffer overlaps an input");
   }
-  if (n == 0) return DDP_OK;
   if (p == 1)  // one scale step, no partials
     return run_fused(in, out, 1, n, dtype, divisor, true, 0, false, stream);
   float* scratch = nullptr;

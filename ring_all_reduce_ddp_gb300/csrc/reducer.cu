@@ -44,6 +44,16 @@ struct ddp_reducer {
   // A rebuild that failed part way leaves no buckets; until a later rebuild
   // succeeds, sync and readiness calls refuse to run rather than do nothing.
   bool unbuilt = false;
+  // Per-forward buffers that ddp_reducer_step broadcasts (kept across
+  // rebuilds). They sit at the end of the piece table as copy pieces; the
+  // in-place sync launches only the first sync_pieces pieces (sync_tiles).
+  std::vector<void*> buf_ptrs;  // [p * kb], replica-major
+  std::vector<int64_t> buf_bytes;
+  int32_t buf_root = 0;
+  int64_t bc_bytes = 0;  // bytes of one replica's buffers
+  int32_t sync_pieces = 0, sync_tiles = 0;
+  // grid cap of the bucket launches mark_ready fires (0: one block per tile)
+  int32_t comm_blocks = 0;
 };
 
 namespace {
@@ -64,6 +74,8 @@ cudaError_t reducer_free_device(ddp_reducer* h) {
   h->table_mem = nullptr;
   h->table = BucketTable{};
   h->table_tiles = 0;
+  h->sync_pieces = 0;
+  h->sync_tiles = 0;
   return first;
 }
 
@@ -97,6 +109,24 @@ ddp_status build_reducer_table(ddp_reducer* h) {
       }
     }
   }
+  const int32_t sync_pieces = static_cast<int32_t>(start.size());
+  const int32_t sync_tiles = tile0.back();
+  // the attached buffers: one copy piece each, root replica = origin - p
+  const int es = esize(h->dt);
+  const int32_t kb = static_cast<int32_t>(h->buf_bytes.size());
+  for (int32_t j = 0; j < kb && p > 1; ++j) {
+    if (h->buf_bytes[j] == 0) continue;
+    const int32_t sl = nslots++;
+    for (int r = 0; r < p; ++r) ptr.push_back(h->buf_ptrs[static_cast<int64_t>(r) * kb + j]);
+    const int64_t n = h->buf_bytes[j] / es;
+    start.push_back(0);
+    len.push_back(n);
+    slot.push_back(sl);
+    origin.push_back(p + h->buf_root);
+    const int64_t t = static_cast<int64_t>(tile0.back()) + (n + tile - 1) / tile;
+    DDP_CHECK(t <= 0x7FFFFFFF, DDP_ERR_ARG, "gradients and buffers too large for one launch");
+    tile0.push_back(static_cast<int32_t>(t));
+  }
   const size_t np = start.size();
   if (np == 0) return DDP_OK;
   auto up16 = [](size_t x) { return (x + 15) / 16 * 16; };
@@ -124,6 +154,8 @@ ddp_status build_reducer_table(ddp_reducer* h) {
   h->table.npieces = static_cast<int>(np);
   h->table.p = p;
   h->table_tiles = tile0.back();
+  h->sync_pieces = sync_pieces;
+  h->sync_tiles = sync_tiles;
   return DDP_OK;
 }
 
@@ -203,7 +235,9 @@ ddp_status reducer_sync_impl(ddp_reducer* h, float divisor, float predivide, ddp
   if (mode == DDP_SYNC_IN_PLACE) {
     DDP_CHECK(algo != DDP_ALGO_RING_STEPS, DDP_ERR_ARG, "the in-place sync is the fused form only");
     DDP_CHECK(predivide == 1.0f, DDP_ERR_ARG, "the in-place sync has no pre-divide");
-    DDP_CUDA(launch_bucket_table(h->table, h->table_tiles, divisor, h->dt, stream), "in-place sync launch");
+    BucketTable sync = h->table;  // the gradient pieces only: the copy pieces come after them
+    sync.npieces = h->sync_pieces;
+    DDP_CUDA(launch_bucket_table(sync, h->sync_tiles, divisor, h->dt, stream), "in-place sync launch");
     return DDP_OK;
   }
   const int es = esize(h->dt);
@@ -239,6 +273,17 @@ ddp_status reducer_sync_impl(ddp_reducer* h, float divisor, float predivide, ddp
   }
   return DDP_OK;
 }
+
+ddp_status reducer_step_impl(ddp_reducer* h, float divisor, cudaStream_t stream) {
+  DDP_NVTX("ddp_reducer_step");
+  DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
+  DDP_TRY(check_divisor(divisor));
+  DDP_CHECK(!h->unbuilt, DDP_ERR_STATE, "the reducer's last rebuild failed; rebuild it again or destroy it");
+  DDP_CUDA(launch_bucket_table(h->table, h->table_tiles, divisor, h->dt, stream), "reducer step launch");
+  return DDP_OK;
+}
+
+int64_t reducer_buffer_bytes(const ddp_reducer* h) { return h ? h->bc_bytes : 0; }
 
 void reducer_shape(const ddp_reducer* h, int32_t* p, ddp_dtype* dt, std::vector<int64_t>* bucket_numel) {
   *p = h ? h->p : 0;
@@ -313,6 +358,73 @@ ddp_status ddp_reducer_destroy(ddp_reducer* h) {
   return DDP_OK;
 }
 
+ddp_status ddp_reducer_set_buffers(ddp_reducer* h, int32_t k, void* const* tensors, const int64_t* nbytes,
+                                   int32_t root) {
+  DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
+  DDP_CHECK(k >= 0, DDP_ERR_ARG, "k must be >= 0");
+  DDP_CHECK(root >= 0 && root < h->p, DDP_ERR_ARG, "root out of range");
+  DDP_CHECK(k == 0 || (tensors && nbytes), DDP_ERR_ARG, "tensors / nbytes arrays are null");
+  DDP_CHECK(!h->unbuilt, DDP_ERR_STATE, "the reducer's last rebuild failed; rebuild it again or destroy it");
+  const int p = h->p, es = esize(h->dt);
+  std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
+  for (int32_t r = 0; r < p; ++r)
+    for (int32_t t = 0; t < h->k; ++t)
+      if (h->numel[t] > 0) ranges.push_back(range_of(h->grads[static_cast<int64_t>(r) * h->k + t], h->numel[t] * es));
+  const size_t ngrad = ranges.size();
+  for (int32_t j = 0; j < k; ++j) {
+    DDP_CHECK(nbytes[j] >= 0, DDP_ERR_ARG, "nbytes must be >= 0");
+    if (nbytes[j] == 0) continue;
+    DDP_CHECK(nbytes[j] % es == 0, DDP_ERR_ARG,
+              "buffer " + std::to_string(j) + ": its bytes must be a multiple of the gradients' element size");
+    for (int32_t r = 0; r < p; ++r) {
+      const void* t = tensors[static_cast<int64_t>(r) * k + j];
+      DDP_CHECK(t != nullptr, DDP_ERR_ARG, "tensors[" + std::to_string(r * k + j) + "] is null");
+      DDP_CHECK(reinterpret_cast<uintptr_t>(t) % es == 0, DDP_ERR_ALIGN,
+                "tensors[" + std::to_string(r * k + j) + "] is not aligned to the gradients' element size");
+      ranges.push_back(range_of(t, nbytes[j]));
+    }
+  }
+  {
+    std::vector<std::pair<uintptr_t, uintptr_t>> bufs(ranges.begin() + ngrad, ranges.end());
+    DDP_CHECK(disjoint(bufs), DDP_ERR_ARG, "buffers overlap");
+  }
+  DDP_CHECK(disjoint(ranges), DDP_ERR_ARG, "a buffer overlaps a gradient of the reducer");
+  // the old table may still be read by launches in flight
+  DDP_CUDA(cudaDeviceSynchronize(), "synchronize before replacing the piece table");
+  h->buf_ptrs.assign(tensors, tensors + static_cast<int64_t>(p) * k);
+  h->buf_bytes.assign(nbytes, nbytes + k);
+  h->buf_root = root;
+  h->bc_bytes = 0;
+  for (int32_t j = 0; j < k && p > 1; ++j) h->bc_bytes += nbytes[j];
+  if (h->table_mem) {
+    DDP_CUDA(cudaFree(h->table_mem), "release of the previous piece table");
+    h->table_mem = nullptr;
+  }
+  h->table = BucketTable{};
+  h->table_tiles = h->sync_pieces = h->sync_tiles = 0;
+  const ddp_status st = build_reducer_table(h);
+  if (st != DDP_OK) {  // keep the handle usable for nothing until a later set or rebuild succeeds
+    const std::string msg = t_error;
+    if (h->table_mem) cudaFree(h->table_mem);
+    h->table_mem = nullptr;
+    h->table = BucketTable{};
+    h->table_tiles = h->sync_pieces = h->sync_tiles = 0;
+    h->buf_ptrs.clear();
+    h->buf_bytes.clear();
+    h->bc_bytes = 0;
+    h->unbuilt = true;
+    return fail(st, msg + " (the reducer has no piece table until a rebuild succeeds)");
+  }
+  return DDP_OK;
+}
+
+ddp_status ddp_reducer_set_comm_blocks(ddp_reducer* h, int32_t max_blocks) {
+  DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
+  DDP_CHECK(max_blocks >= 0, DDP_ERR_ARG, "max_blocks must be >= 0");
+  h->comm_blocks = max_blocks;
+  return DDP_OK;
+}
+
 ddp_status ddp_reducer_prepare(ddp_reducer* h) {
   DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
   DDP_CHECK(!h->unbuilt, DDP_ERR_STATE, "the reducer's last rebuild failed; rebuild it again or destroy it");
@@ -343,7 +455,7 @@ ddp_status ddp_reducer_mark_ready(ddp_reducer* h, int32_t tensor, float divisor,
       DDP_CUDA(cudaStreamWaitEvent(comm_stream, ready, 0), "wait on the gradient's ready event");
       waited = true;
     }
-    DDP_TRY(run_bucket_launches(h->buckets[h->next_bucket].launches, h->dt, divisor, comm_stream));
+    DDP_TRY(run_bucket_launches(h->buckets[h->next_bucket].launches, h->dt, divisor, comm_stream, h->comm_blocks));
     ++h->next_bucket;
     ++n;
   }

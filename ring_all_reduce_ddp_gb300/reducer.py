@@ -15,8 +15,8 @@ from __future__ import annotations
 
 import ctypes
 
-from . import (DDP_ALGO_FUSED, DDP_ORDER_REVERSED, DDP_SYNC_IN_PLACE, DDPReducer, _ptrs, _i64s,
-               ddp_broadcast_coalesced, ddp_bucket_assign, ddp_bucket_assign_order)
+from . import (DDP_ALGO_FUSED, DDP_ORDER_REVERSED, DDP_SYNC_IN_PLACE, DDPReducer, _check, _ptrs, _i64s,
+               ddp_broadcast_coalesced, ddp_bucket_assign, ddp_bucket_assign_order, lib)
 
 MiB = 1 << 20
 
@@ -39,14 +39,40 @@ class Reducer(DDPReducer):
         self.bucket_numel = plan["bucket_numel"]
         self.offset = plan["offset"]
         assert self.num_buckets() == len(self.buckets)
+        self._prepare_assign()
+
+    def _prepare_assign(self):
+        """The argument and result arrays of the per-step assignment call, made
+        once, and the plan's CSR arrays to compare its result with."""
+        k = len(self.numel)
+        self._a_numel = _i64s(self.numel)
+        self._a_nb = ctypes.c_int32(0)
+        self._a_of = (ctypes.c_int32 * max(1, k))()
+        self._a_off = (ctypes.c_int64 * max(1, k))()
+        self._a_ptr = (ctypes.c_int32 * (k + 1))()
+        self._a_tens = (ctypes.c_int32 * max(1, k))()
+        self._a_bn = (ctypes.c_int64 * max(1, k))()
+        self._a_walk = None if self._walk is None else (ctypes.c_int32 * max(1, k))(*[int(x) for x in self._walk])
+        ptr, tens = [0], []
+        for b in self.buckets:
+            tens += b
+            ptr.append(len(tens))
+        self._want = (len(self.buckets), bytes((ctypes.c_int32 * (k + 1))(*ptr))[:4 * (len(self.buckets) + 1)],
+                      bytes((ctypes.c_int32 * max(1, k))(*tens))[:4 * len(tens)])
 
     def assign(self) -> bool:
-        """Recompute the bucket assignment (host only); True if it is unchanged."""
-        if self._walk is not None:
-            got = ddp_bucket_assign_order(self.numel, self.esize, self._caps[0], self._caps[1], self._walk)
+        """Recompute the bucket assignment (host only, ddp_bucket_assign or,
+        after a rebuild, ddp_bucket_assign_order); True if it is unchanged."""
+        k = len(self.numel)
+        head = (k, self._a_numel, self.esize, self._caps[0], self._caps[1])
+        tail = (ctypes.byref(self._a_nb), self._a_of, self._a_off, self._a_ptr, self._a_tens, self._a_bn)
+        if self._a_walk is not None:
+            _check(lib().ddp_bucket_assign_order(*head, self._a_walk, *tail))
         else:
-            got = ddp_bucket_assign(self.numel, self.esize, *self._caps)
-        return got["buckets"] == self.buckets
+            _check(lib().ddp_bucket_assign(*head, self._caps[2], *tail))
+        nb = self._a_nb.value
+        return (nb == self._want[0] and bytes(self._a_ptr)[:4 * (nb + 1)] == self._want[1]
+                and bytes(self._a_tens)[:len(self._want[2])] == self._want[2])
 
     def rebuild(self, order=None):
         """Rebuild the buckets along `order`, or along the ready order observed
@@ -60,6 +86,7 @@ class Reducer(DDPReducer):
         self.bucket_numel = plan["bucket_numel"]
         self.offset = plan["offset"]
         assert self.num_buckets() == len(self.buckets)
+        self._prepare_assign()
 
     def sync_gradients(self, divisor: float, algo: int = DDP_ALGO_FUSED, mode: int = DDP_SYNC_IN_PLACE,
                        predivide: float = 1.0, stream=None):

@@ -52,6 +52,17 @@ def esize(cfg) -> int:
     return 4 if cfg["dtype"] == "f32" else 2
 
 
+def arena_layout(cfg):
+    """Element offset of each tensor inside a replica's arena (256-byte
+    aligned, registration order) and the arena's length in elements."""
+    align = 256 // esize(cfg)
+    offs, pos = [], 0
+    for x in numels(cfg):
+        offs.append(pos)
+        pos += (x + align - 1) // align * align
+    return offs, pos
+
+
 def make_grads(cfg, device="cuda", p=None):
     """p lists of k device tensors holding the seeded gradients."""
     import torch
@@ -59,11 +70,7 @@ def make_grads(cfg, device="cuda", p=None):
     tdt = torch.float32 if cfg["dtype"] == "f32" else torch.bfloat16
     n = numels(cfg)
     starts = tensor_starts(cfg)
-    align = 256 // esize(cfg)
-    offs, pos = [], 0
-    for x in n:
-        offs.append(pos)
-        pos += (x + align - 1) // align * align
+    offs, pos = arena_layout(cfg)
     grads, arenas = [], []
     for r in range(p):
         arena = torch.empty(max(pos, 1), dtype=tdt, device=device)
@@ -73,6 +80,28 @@ def make_grads(cfg, device="cuda", p=None):
             fill_(v, "normal", cfg["seed"], r, starts[t], cfg["sigma"])
             row.append(v)
         grads.append(row)
+        arenas.append(arena)
+    return grads, arenas
+
+
+def make_grads_from_host(cfg, device="cuda", p=None):
+    """As make_grads, with the same values and layout, but every replica's
+    arena is generated on the host and copied to the device in one copy, so no
+    device kernel runs (for small sets)."""
+    import torch
+    p = p or cfg["p"]
+    n = numels(cfg)
+    starts = tensor_starts(cfg)
+    offs, pos = arena_layout(cfg)
+    host_dt = np.float32 if cfg["dtype"] == "f32" else np.uint16
+    grads, arenas = [], []
+    for r in range(p):
+        h = np.zeros(max(pos, 1), dtype=host_dt)
+        for t, x in enumerate(n):
+            h[offs[t]:offs[t] + x] = host_values(cfg, r, np.arange(starts[t], starts[t] + x))
+        ht = torch.from_numpy(h) if cfg["dtype"] == "f32" else torch.from_numpy(h.view(np.int16)).view(torch.bfloat16)
+        arena = ht.to(device)
+        grads.append([arena[offs[t]:offs[t] + x] for t, x in enumerate(n)])
         arenas.append(arena)
     return grads, arenas
 
@@ -104,5 +133,29 @@ def buffer_set(cfg, device="cuda", p=None):
                 else:
                     t = torch.full(shp, r * 1000 + j, dtype=torch.int64, device=device)
                 row.append(t)
+        out.append(row)
+    return out
+
+
+def buffer_set_host(cfg, p=None):
+    """The bytes of buffer_set's tensors, generated on the host: p lists of
+    uint8 arrays, the same values buffer_set puts on the device."""
+    p = p or cfg["p"]
+    kind = cfg.get("buffers")
+    out = []
+    for r in range(p):
+        row = []
+        if kind == "llama":
+            for j, s in enumerate(S.llama_buffers()):
+                v = values_np("uniform", cfg["seed"] + 7, 1000 + r * 64 + j, np.arange(s))
+                row.append(v.view(np.uint8).copy())
+        elif kind == "resnet50":
+            for j, (_, shp, dt) in enumerate(S.resnet50_buffers()):
+                n = S.numel(shp)
+                if dt == "f32":
+                    v = values_np("uniform", cfg["seed"] + 7, 1000 + r * 1000 + j, np.arange(n))
+                else:
+                    v = np.full(n, r * 1000 + j, dtype=np.int64)
+                row.append(v.view(np.uint8).copy())
         out.append(row)
     return out

@@ -35,17 +35,38 @@ def test_reference_arm_line():
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["same_config"] is True  # a few tiny steps: the whole step every time
+
+
+def test_reference_arm_times_the_gpu_arms_step_bytes():
+    """The oracle's step is credited with the bytes the GPU arm's in-place step
+    is credited with: 2pM for the sync and pB for the buffers' broadcast."""
+    import bench
+    from synth import workloads as W
+    from synth import shapes as S
+    cfg = W.CONFIGS["resnet50"]
+    M = sum(W.numels(cfg)) * 4
+    B = sum(4 * S.numel(shp) if dt == "f32" else 8 * S.numel(shp) for _, shp, dt in S.resnet50_buffers())
+    assert bench.oracle_step_bytes(cfg) == 2 * 8 * M + 8 * B
+    tiny = W.CONFIGS["tiny"]
+    assert bench.oracle_step_bytes(tiny) == 2 * 4 * sum(W.numels(tiny)) * 4
 
 
 @pytest.mark.gpu
 def test_gpu_arm_line():
-    d = _run(["--steps", "64", "--warmup", "3", "--no-cpu-baseline"])
+    d = _run(["--steps", "20", "--warmup", "3", "--no-cpu-baseline"])
     _base(d)
     assert d["metric"] and d["value"] > 0 and d["dtype"] == "f32"
     r = d["roofline"]
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0 < r["frac"] < 1.2 and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    assert r["event_timed_launches"] >= 32
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
-    assert d["gpu_launches"] == 2 * 64  # the buffer broadcast and the sync, every step
+    assert d["gpu_launches"] == 20  # the buffer broadcast and the sync: one launch every step
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    pts = d["sweep"]["points"]
+    assert {(x["p"], x["bytes"] >> 20) for x in pts} == {(p, m) for p in (2, 8, 64) for m in (1, 25, 256)}
+    assert all(x["gbs"] > 0 and abs(x["frac"] - x["gbs"] / r["peak"]) < 1e-3 for x in pts)
+    assert set(d["configs"]) == {"gpt2_small", "llama_1b"}
+    assert all(c["us"] > 0 and c["buckets_per_s"] > 0 for c in d["configs"].values())

@@ -15,7 +15,8 @@ from oracle import ring as orc
 from oracle.bf16 import bf16_to_f32
 from ring_all_reduce_ddp_gb300.reducer import Reducer, broadcast_buffers
 from synth import workloads as W
-from tests.helpers import assert_bf16_close, assert_bit_equal, make_replicas, to_host
+from tests.helpers import assert_bit_equal, make_replicas, to_host
+from tests.oracle_sync import check_sync_sampled, check_whole_set, oracle_plan
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -175,78 +176,8 @@ def test_broadcast_handle_tree_steps(p, root):
 
 
 # ------------------------------------------------------------- whole syncs
-def _sample(n, cs_p, tensor_bounds, rng, k=2000):
-    idx = set(range(min(n, 64))) | set(range(max(0, n - 64), n))
-    p = cs_p[1]
-    cs = cs_p[0]
-    for c in range(p + 1):
-        for d in (-2, -1, 0, 1, 2):
-            i = c * cs + d
-            if 0 <= i < n:
-                idx.add(i)
-    for b in tensor_bounds:
-        for d in (-2, -1, 0, 1, 2):
-            if 0 <= b + d < n:
-                idx.add(b + d)
-    idx |= set(int(x) for x in rng.integers(0, n, size=min(k, n)))
-    return np.array(sorted(idx), dtype=np.int64)
-
-
-def _check_sync_sampled(cfg, red, grads, rng, per_bucket=2000):
-    """Compare the synchronised gradients with the oracle on sampled elements of every bucket."""
-    p = cfg["p"]
-    starts = W.tensor_starts(cfg)
-    numel = W.numels(cfg)
-    Dv = W.divisor(cfg)
-    for b, members in enumerate(red.buckets):
-        n = red.bucket_numel[b]
-        offs = [red.offset[t] for t in members]
-        idx = _sample(n, (orc.chunk_size(n, p), p), offs, rng, per_bucket)
-        # element i of the bucket is element i - offset[t] of tensor t
-        which = np.searchsorted(np.array(offs), idx, side="right") - 1
-        tens = np.array(members)[which]
-        within = idx - np.array(offs)[which]
-        flat_idx = np.array(starts)[tens] + within
-        ins = [W.host_values(cfg, r, flat_idx) for r in range(p)]
-        want, _ = orc.allreduce(ins, n, Dv, cfg["dtype"], idx=idx)
-        for r in range(p):
-            got = np.empty(idx.size, dtype=want[r].dtype)
-            for t in np.unique(tens):
-                sel = tens == t
-                vals = grads[r][t].view(-1)[torch.from_numpy(within[sel]).cuda()]
-                got[sel] = to_host(vals)
-            assert_bit_equal(got, want[r], f"bucket {b} replica {r}")
-            if cfg["dtype"] == "bf16":
-                assert_bf16_close(got, want[r])
-    return True
-
-
 SYNCS = [(D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE), (D.DDP_ALGO_FUSED, D.DDP_SYNC_FLATTEN),
          (D.DDP_ALGO_FUSED_TMA, D.DDP_SYNC_FLATTEN), (D.DDP_ALGO_RING_STEPS, D.DDP_SYNC_FLATTEN)]
-
-
-def _tiny_expected(cfg, red):
-    """Oracle: flatten, literal ring all-reduce, unflatten, per bucket; tensor -> values per replica."""
-    p = cfg["p"]
-    numel = W.numels(cfg)
-    starts = W.tensor_starts(cfg)
-    out = [dict() for _ in range(p)]
-    for b, members in enumerate(red.buckets):
-        n = red.bucket_numel[b]
-        ins = []
-        for r in range(p):
-            hv = {t: W.host_values(cfg, r, np.arange(starts[t], starts[t] + numel[t])) for t in members}
-            if cfg["dtype"] == "bf16":
-                hv = {t: bf16_to_f32(v) for t, v in hv.items()}
-            ins.append(ob.flatten([hv.get(t, np.zeros(0, np.float32)) for t in range(len(numel))], members,
-                                  red.offset, n))
-        if cfg["dtype"] == "bf16":
-            from oracle.bf16 import f32_to_bf16
-            ins = [f32_to_bf16(x) for x in ins]
-        want, _ = orc.allreduce(ins, n, W.divisor(cfg), cfg["dtype"])
-        for r in range(p):
-            out[r].update(ob.unflatten(want[r], members, red.offset, numel))
-    return out
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -261,10 +192,7 @@ def test_tiny_ddp_sync_full_parity(algo, mode, dtype):
         assert red.buckets == [[9, 8], [7, 6, 5, 4, 3, 2, 1, 0]]
     red.sync_gradients(W.divisor(cfg), algo, mode)
     torch.cuda.synchronize()
-    want = _tiny_expected(cfg, red)
-    for r in range(p):
-        for t in range(len(grads[r])):
-            assert_bit_equal(to_host(grads[r][t]), want[r][t], f"tensor {t} replica {r}")
+    check_whole_set(cfg, red, grads)
     assert D.ddp_device_error() == 0
 
 
@@ -291,10 +219,7 @@ def test_tiny_ddp_sync_replicas_misaligned_differently(algo, mode, dtype):
     red = Reducer(grads, cfg["first_cap"], cfg["cap"])
     red.sync_gradients(W.divisor(cfg), algo, mode)
     torch.cuda.synchronize()
-    want = _tiny_expected(cfg, red)
-    for r in range(p):
-        for t in range(len(grads[r])):
-            assert_bit_equal(to_host(grads[r][t]), want[r][t], f"tensor {t} replica {r}")
+    check_whole_set(cfg, red, grads)
     assert D.ddp_device_error() == 0
 
 
@@ -351,6 +276,23 @@ def test_bucket_allreduce_in_place_matches_flatten_path_oracle(p, dtype, skew):
     assert D.ddp_device_error() == 0
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("p", [2, 3, 16, 17, 64])
+def test_in_place_sync_every_replica_count_branch(p, dtype):
+    """The whole-Reducer in-place sync (one launch over the device-resident
+    piece table) at replica counts that take each of its compiled forms: p = 2
+    and 16 unrolled, 3, 17 and 64 the generic loop (p = 4 and 8 run in the
+    tests above). The tiny set's ten tensors on p replicas, every element
+    against the oracle's flatten + ring + unflatten on the oracle's own plan."""
+    cfg = dict(W.CONFIGS["tiny"], dtype=dtype, p=p)
+    grads, _ = W.make_grads(cfg, p=p)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE)
+    torch.cuda.synchronize()
+    check_whole_set(cfg, red, grads)
+    assert D.ddp_device_error() == 0
+
+
 @pytest.mark.parametrize("mode", [D.DDP_SYNC_IN_PLACE, D.DDP_SYNC_FLATTEN])
 @pytest.mark.parametrize("name", ["resnet50", "gpt2_small"])
 def test_model_sized_sync_sampled_parity(name, mode):
@@ -360,7 +302,7 @@ def test_model_sized_sync_sampled_parity(name, mode):
     red = Reducer(grads, cfg["first_cap"], cfg["cap"])
     red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED, mode)
     torch.cuda.synchronize()
-    _check_sync_sampled(cfg, red, grads, np.random.default_rng(5))
+    check_sync_sampled(cfg, red, grads, np.random.default_rng(5))
     # every replica ends identical (the data-parallel invariant), on whole tensors
     for t in range(len(grads[0])):
         for r in range(1, cfg["p"]):
@@ -383,7 +325,7 @@ def test_llama_bf16_sync_and_buffer_broadcast_sampled_parity():
     assert len(red.buckets) == 66
     red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED)
     torch.cuda.synchronize()
-    _check_sync_sampled(cfg, red, grads, np.random.default_rng(6), per_bucket=300)
+    check_sync_sampled(cfg, red, grads, np.random.default_rng(6), per_bucket=300)
     assert D.ddp_device_error() == 0
 
 
@@ -408,20 +350,17 @@ def test_sync_reads_what_the_kernel_before_it_wrote(name):
         red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE, 1.0, s)
         if rep == 0:
             torch.cuda.synchronize()
-            _, offset, bnumel = ob.bucket_layout(numel, red.buckets)
+            buckets, offset, bnumel = oracle_plan(cfg, red)
             rng = np.random.default_rng(11)
-            for b, members in enumerate(red.buckets):
+            for b, members in enumerate(buckets):
                 t = members[int(rng.integers(0, len(members)))]
                 idx = np.unique(np.concatenate([np.arange(min(64, numel[t])),
                                                 rng.integers(0, numel[t], size=min(512, numel[t]))]))
                 x0 = W.host_values(cfg, 0, starts[t] + idx)
-                # every replica holds replica 0's values: fold p copies in fp32, divide once
-                acc = x0.copy()
-                for _ in range(p - 1):
-                    acc = (acc + x0).astype(np.float32)
-                want = (acc / np.float32(W.divisor(cfg))).astype(np.float32)
+                # every replica holds replica 0's values: the oracle's ring over p copies of them
+                want, _ = orc.allreduce([x0] * p, bnumel[b], W.divisor(cfg), cfg["dtype"], idx=offset[t] + idx)
                 for r in range(p):
-                    assert_bit_equal(to_host(grads[r][t])[idx], want, f"tensor {t} replica {r}")
+                    assert_bit_equal(to_host(grads[r][t])[idx], want[r], f"tensor {t} replica {r}")
     torch.cuda.synchronize()
     for t in range(len(numel)):
         for r in range(1, p):
@@ -449,18 +388,16 @@ def test_ready_firing_reads_what_the_kernel_before_it_wrote(name):
         assert fired == len(red.buckets)
         if rep == 0:
             torch.cuda.synchronize()
+            buckets, offset, bnumel = oracle_plan(cfg, red)
             rng = np.random.default_rng(12)
-            for members in red.buckets:
+            for b, members in enumerate(buckets):
                 for t in members:
                     idx = np.unique(np.concatenate([np.arange(min(64, numel[t])),
                                                     rng.integers(0, numel[t], size=min(256, numel[t]))]))
                     x0 = W.host_values(cfg, 0, starts[t] + idx)
-                    acc = x0.copy()
-                    for _ in range(p - 1):
-                        acc = (acc + x0).astype(np.float32)
-                    want = (acc / np.float32(Dv)).astype(np.float32)
+                    want, _ = orc.allreduce([x0] * p, bnumel[b], Dv, cfg["dtype"], idx=offset[t] + idx)
                     for r in range(p):
-                        assert_bit_equal(to_host(grads[r][t])[idx], want, f"tensor {t} replica {r}")
+                        assert_bit_equal(to_host(grads[r][t])[idx], want[r], f"tensor {t} replica {r}")
     torch.cuda.synchronize()
     for t in range(len(numel)):
         for r in range(1, p):

@@ -16,6 +16,7 @@ from oracle import ring as orc
 from ring_all_reduce_ddp_gb300.reducer import Reducer
 from synth import workloads as W
 from tests.helpers import assert_bit_equal, to_host
+from tests.oracle_sync import check_sync_sampled, check_whole_set, oracle_plan
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -33,12 +34,20 @@ def _fire_positions(red, order, divisor, comm, compute):
     return seq
 
 
+@pytest.mark.parametrize("comm_blocks", [0, 5, 96])
+@pytest.mark.parametrize("name", ["tiny", "resnet50"])
 @pytest.mark.parametrize("shuffle", [False, True])
-def test_mark_ready_fires_like_the_reducer_and_reduces_like_a_sync(shuffle):
-    cfg = W.CONFIGS["resnet50"]
+def test_mark_ready_fires_like_the_reducer_and_reduces_like_the_oracle(name, shuffle, comm_blocks):
+    """Firing positions against the oracle's replay; values against the
+    oracle's ring on the oracle's own bucket plan (every element of the tiny
+    set, sampled elements of the ResNet-50-shaped one) and against a
+    whole-set sync of the same inputs. With a grid cap the bucket launches
+    stride over their tiles with that many blocks: the same bits."""
+    cfg = W.CONFIGS[name]
     grads, _ = W.make_grads(cfg)
     ref_grads, _ = W.make_grads(cfg)
     red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    red.set_comm_blocks(comm_blocks)
     ref = Reducer(ref_grads, cfg["first_cap"], cfg["cap"])
     Dv = W.divisor(cfg)
     ref.sync_gradients(Dv, D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE)
@@ -51,8 +60,13 @@ def test_mark_ready_fires_like_the_reducer_and_reduces_like_a_sync(shuffle):
     red.prepare()
     seq = _fire_positions(red, order, Dv, comm, compute)
     torch.cuda.synchronize()
-    assert seq == rs.fire_sequence(red.buckets, order)
+    plan, _, _ = oracle_plan(cfg, red)
+    assert seq == rs.fire_sequence(plan, order)
     assert red.observed() == order
+    if name == "tiny":
+        check_whole_set(cfg, red, grads)
+    else:
+        check_sync_sampled(cfg, red, grads, np.random.default_rng(4), per_bucket=1000)
     for r in range(cfg["p"]):
         for t in range(k):
             assert torch.equal(grads[r][t].view(torch.int32), ref_grads[r][t].view(torch.int32)), (r, t)
@@ -74,9 +88,11 @@ def test_rebuild_from_the_observed_order():
     for t in observed:  # readiness only: the in-place reduction of this pass is checked above
         red.mark_ready(t, 1.0, None, comm)
     torch.cuda.synchronize()
+    assert red.assign()  # the per-step host check of the default plan
     red.rebuild()  # along the observed order
     want_buckets = rs.rebuild(numel, 4, cfg["first_cap"], cfg["cap"], observed)
     assert red.buckets == want_buckets
+    assert red.assign()  # and of the rebuilt one
     # fresh gradients, one sync on the rebuilt buckets, every element against the oracle
     fresh, _ = W.make_grads(cfg)
     for r in range(p):
@@ -186,3 +202,12 @@ def test_collectives_capture_into_cuda_graphs(dtype):
             assert torch.equal(outs_g[r].view(view), outs_e[r].view(view)), (op, algo, r)
         del g
     assert D.ddp_device_error() == 0
+
+
+def test_comm_blocks_must_not_be_negative():
+    cfg = W.CONFIGS["tiny"]
+    grads, _ = W.make_grads(cfg)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    with pytest.raises(D.DDPError) as e:
+        red.set_comm_blocks(-1)
+    assert e.value.status == D.DDP_ERR_ARG

@@ -69,6 +69,73 @@ def test_hierarchical_traffic_is_smaller():
     assert costs.hierarchical_net_bytes(M, 1, g) == 0
 
 
+def test_hierarchical_traffic_hand_worked():
+    """2 nodes of 8 GPUs, 1 GB: after the in-node reduce-scatter each GPU holds
+    M/8 = 125 MB and runs a 2-rank ring across nodes, sending 2(2-1)/2 of it:
+    125 MB. The flat ring over all 16 GPUs sends 2 * 15/16 GB = 1.875 GB."""
+    assert costs.hierarchical_net_bytes(1e9, 2, 8) == pytest.approx(125e6, rel=1e-15)
+    assert costs.flat_ring_net_bytes(1e9, 2, 8) == pytest.approx(1.875e9, rel=1e-15)
+    assert costs.hierarchical_net_bytes(1e9, 4, 8) == pytest.approx(187.5e6, rel=1e-15)
+
+
+@pytest.mark.parametrize("n,g", [(2, 8), (4, 8), (3, 4), (8, 2)])
+def test_hierarchical_traffic_equals_the_simulated_cross_node_ring(n, g):
+    """The cross-node phase of the hierarchical all-reduce is a ring all-reduce
+    of each GPU's M/g shard among the n nodes: the oracle's simulated ring
+    counts the bytes one rank sends, which must equal the closed form."""
+    M_elems = 1024 * n * g  # fp32 elements, so M/g divides into n chunks
+    shard = M_elems // g
+    bufs = [np.ones(shard, np.float32) for _ in range(n)]
+    _, info = orc.allreduce(bufs, shard, 1.0, "f32")
+    per_rank = set(info["bytes_sent"])
+    assert per_rank == {costs.hierarchical_net_bytes(4 * M_elems, n, g)}
+    flat = [np.ones(M_elems, np.float32) for _ in range(n * g)]
+    _, finfo = orc.allreduce(flat, M_elems, 1.0, "f32")
+    assert set(finfo["bytes_sent"]) == {costs.flat_ring_net_bytes(4 * M_elems, n, g)}
+
+
+@pytest.mark.parametrize("p", [2, 3, 8, 16])
+def test_bus_bandwidth_is_the_simulated_per_rank_send_rate(p):
+    """Bus bandwidth is what one rank's link carries: the bytes the simulated
+    ring makes a rank send, divided by the time. Given the algorithm bandwidth
+    M / t of the same all-reduce, bus_bandwidth must reproduce it."""
+    n = 96 * p  # divisible by p: no padding on the wire
+    M = 4 * n
+    bufs = [np.full(n, r, np.float32) for r in range(p)]
+    _, info = orc.allreduce(bufs, n, 1.0, "f32")
+    for t in (1e-6, 3.7e-3, 2.0):
+        for sent in info["bytes_sent"]:
+            assert costs.bus_bandwidth(M / t, p) == pytest.approx(sent / t, rel=1e-12)
+
+
+def test_example_gradient_hand_worked():
+    """x = (1, 2), w = (3, 4), y = 5: the residual is 11 - 5 = 6, so the
+    gradient of 0.5 (x.w - y)^2 is 6 x = (6, 12)."""
+    g = linear_dp.example_grads(np.array([[1.0, 2.0]]), np.array([5.0]), np.array([3.0, 4.0]))
+    assert np.array_equal(g, np.array([[6.0, 12.0]]))
+
+
+def test_example_gradients_are_the_loss_derivative():
+    """Central finite differences of each example's loss 0.5 (x.w - y)^2 give
+    its gradient row; the batch mean gradient is zero at the least-squares
+    solution (the normal equations)."""
+    rng = np.random.default_rng(7)
+    X = rng.standard_normal((9, 5))
+    y = rng.standard_normal(9)
+    w = rng.standard_normal(5)
+    G = linear_dp.example_grads(X, y, w)
+    h = 1e-6
+    for i in range(X.shape[0]):
+        for j in range(X.shape[1]):
+            e = np.zeros(5)
+            e[j] = h
+            lp = 0.5 * (X[i] @ (w + e) - y[i]) ** 2
+            lm = 0.5 * (X[i] @ (w - e) - y[i]) ** 2
+            assert G[i, j] == pytest.approx((lp - lm) / (2 * h), rel=1e-6, abs=1e-8)
+    w_star = np.linalg.lstsq(X, y, rcond=None)[0]
+    assert np.allclose(linear_dp.batch_mean_grad(X, y, w_star), 0.0, atol=1e-12)
+
+
 def _shards(rng, counts, d=6):
     w = rng.standard_normal(d)
     shards = []

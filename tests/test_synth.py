@@ -40,3 +40,15 @@ def test_shape_sets():
     assert (len(shapes.llama_1b()), sum(shapes.numel(s) for _, s in shapes.llama_1b())) == (147, 1204881408)
     b = shapes.llama_buffers()
     assert len(b) == 64 and all(256 <= v <= 4096 for v in b)
+
+
+def test_host_buffer_set_matches_the_device_one():
+    from synth import workloads as W
+    for name in ("resnet50", "llama_1b"):
+        cfg = W.CONFIGS[name]
+        dev = W.buffer_set(cfg, "cpu", p=2)
+        host = W.buffer_set_host(cfg, p=2)
+        for r in range(2):
+            assert len(dev[r]) == len(host[r])
+            for d, h in zip(dev[r], host[r]):
+                assert np.array_equal(d.contiguous().view(-1).view(torch.uint8).numpy(), h)
