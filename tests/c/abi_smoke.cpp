@@ -79,7 +79,7 @@ int main() {
     }
   }
 
-  // a Reducer over two tensors per replica, whole-set sync in place
+  // a Reducer over two tensors per replica, whole-set sync in place, then the one-launch step
   {
     const int p = 2, k = 2;
     const int64_t numel[k] = {300, 5000};
@@ -105,8 +105,33 @@ int main() {
         const float want = (10.0f + t + 20.0f + t) / 2.0f;
         for (int64_t i = 0; i < numel[t]; ++i) CHECK(v[i] == want, "reducer value");
       }
+    // one buffer per replica attached: the step copies replica 1's to replica 0 and syncs again
+    const int64_t nb = 64;
+    std::vector<void*> bufs(p);
+    for (int r = 0; r < p; ++r) {
+      CHECK(cudaMalloc(&bufs[r], nb * sizeof(float)) == cudaSuccess, "cudaMalloc buffer");
+      std::vector<float> v(nb, static_cast<float>(100 + r));
+      CHECK(cudaMemcpy(bufs[r], v.data(), nb * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess, "upload buffer");
+    }
+    const int64_t nbytes[1] = {nb * static_cast<int64_t>(sizeof(float))};
+    CHECK(ddp_reducer_set_buffers(h, 1, bufs.data(), nbytes, 1) == DDP_OK, "ddp_reducer_set_buffers");
+    CHECK(ddp_reducer_step(h, 1.0f, s) == DDP_OK, "ddp_reducer_step");
+    CHECK(cudaStreamSynchronize(s) == cudaSuccess, "sync");
+    for (int r = 0; r < p; ++r) {
+      std::vector<float> v(nb);
+      CHECK(cudaMemcpy(v.data(), bufs[r], nb * sizeof(float), cudaMemcpyDeviceToHost) == cudaSuccess, "download buffer");
+      for (int64_t i = 0; i < nb; ++i) CHECK(v[i] == 101.0f, "buffer broadcast from replica 1");
+      for (int t = 0; t < k; ++t) {
+        std::vector<float> g(numel[t]);
+        CHECK(cudaMemcpy(g.data(), grads[r * k + t], numel[t] * sizeof(float), cudaMemcpyDeviceToHost) == cudaSuccess,
+              "download grad");
+        const float want = 2.0f * (10.0f + t + 20.0f + t) / 2.0f;  // two equal copies summed, divisor 1
+        for (int64_t i = 0; i < numel[t]; ++i) CHECK(g[i] == want, "step value");
+      }
+    }
     CHECK(ddp_reducer_destroy(h) == DDP_OK, "ddp_reducer_destroy");
     for (void* g : grads) cudaFree(g);
+    for (void* b : bufs) cudaFree(b);
   }
 
   // errors come back as codes, with this thread's text
