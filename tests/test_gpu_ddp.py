@@ -310,21 +310,30 @@ def test_model_sized_sync_sampled_parity(name, mode):
     assert D.ddp_device_error() == 0
 
 
-def test_llama_bf16_sync_and_buffer_broadcast_sampled_parity():
+@pytest.mark.parametrize("one_launch", [False, True])
+def test_llama_bf16_sync_and_buffer_broadcast_sampled_parity(one_launch):
     """1.2B bf16 gradients on 8 replicas (about 39 GB with the buckets), and the
-    per-forward broadcast of 64 fp32 buffers from replica 0."""
+    per-forward broadcast of 64 fp32 buffers from replica 0: as two calls (the
+    coalesced broadcast, then the in-place sync) and as the one-launch step
+    the bench's configs field times. Buffers against the oracle's coalesced
+    broadcast of the host-generated bytes."""
     cfg = W.CONFIGS["llama_1b"]
     bufs = W.buffer_set(cfg)
-    root_bytes = [b.cpu().numpy().view(np.uint8).copy() for b in bufs[0]]
-    broadcast_buffers(bufs, 0)
-    for r in range(cfg["p"]):
-        for j, b in enumerate(bufs[r]):
-            assert np.array_equal(b.cpu().numpy().view(np.uint8), root_bytes[j])
+    host = W.buffer_set_host(cfg)
+    want_bufs, _ = orc.broadcast_coalesced(host, 0)
     grads, _ = W.make_grads(cfg)
     red = Reducer(grads, cfg["first_cap"], cfg["cap"])
     assert len(red.buckets) == 66
-    red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED)
+    if one_launch:
+        red.set_buffers(bufs, 0)
+        red.step(W.divisor(cfg))
+    else:
+        broadcast_buffers(bufs, 0)
+        red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED)
     torch.cuda.synchronize()
+    for r in range(cfg["p"]):
+        for j, b in enumerate(bufs[r]):
+            assert np.array_equal(b.cpu().numpy().view(np.uint8), want_bufs[r][j]), (r, j)
     check_sync_sampled(cfg, red, grads, np.random.default_rng(6), per_bucket=300)
     assert D.ddp_device_error() == 0
 

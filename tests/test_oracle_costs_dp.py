@@ -177,3 +177,27 @@ def test_ring_with_token_count_divisor_gives_the_batch_gradient():
     outs, _ = orc.allreduce(bufs, 23, float(sum(counts)), "f64")
     for o in outs:
         assert np.allclose(o, full, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("p", [2, 3, 4, 8, 16])
+def test_per_rank_byte_forms_equal_the_simulated_schedules(p):
+    """The closed forms of what one rank sends, against the oracle's simulated
+    byte counters (n divisible by p, so no padding goes on the wire): the
+    two-pass ring sends 2(p-1)/p of the tensor per rank and meets the lower
+    bound; each of its halves sends (p-1)/p; recursive doubling's time with
+    no latency term is its per-rank bytes, M log2 p, times beta."""
+    from oracle import trees
+    n = 40 * p
+    M = 4 * n
+    bufs = [np.full(n, r + 1, np.float32) for r in range(p)]
+    _, ar = orc.allreduce(bufs, n)
+    assert set(ar["bytes_sent"]) == {costs.ring_bytes_per_rank(M, p)} == {costs.lower_bound_bytes(M, p)}
+    _, rs = orc.reduce_scatter(bufs, n, 1.0, "f32", "ring")
+    assert set(rs["bytes_sent"]) == {costs.half_bytes_per_rank(M, p)}
+    _, ag = orc.allgather([np.full(n // p, r, np.float32) for r in range(p)])
+    assert set(ag["bytes_sent"]) == {costs.half_bytes_per_rank(M, p)}
+    if p & (p - 1) == 0:
+        _, rd = trees.recursive_doubling(bufs, n)
+        beta = 1e-9
+        for sent in rd["bytes_sent"]:
+            assert costs.recursive_doubling_time(M, p, 0.0, beta) == pytest.approx(sent * beta, rel=1e-12)
