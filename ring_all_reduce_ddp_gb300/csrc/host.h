@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <string>
 #include <utility>
@@ -38,15 +39,23 @@ extern thread_local std::string t_error;  // this thread's last error text (ddp_
   } while (0)
 
 // One NVTX range per C-ABI call that enqueues device work, named after the
-// entry point, for timeline tools and ncu's --nvtx filters. Without a tool
-// attached a range costs a pointer check.
+// entry point, and nested ones per literal ring step and per bucket, for
+// timeline tools and ncu's --nvtx filters. Without a tool attached a range
+// costs a pointer check.
 struct NvtxRange {
   explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  // "<what> <i>", e.g. "bucket 3" or "reduce-scatter step 2"
+  NvtxRange(const char* what, int i) {
+    char buf[64];
+    std::snprintf(buf, sizeof(buf), "%s %d", what, i);
+    nvtxRangePushA(buf);
+  }
   ~NvtxRange() { nvtxRangePop(); }
   NvtxRange(const NvtxRange&) = delete;
   NvtxRange& operator=(const NvtxRange&) = delete;
 };
 #define DDP_NVTX(name) ::ddp::host::NvtxRange nvtx_range_(name)
+#define DDP_NVTX_I(what, i) ::ddp::host::NvtxRange nvtx_range_i_(what, i)
 
 struct Plan;
 
@@ -130,6 +139,10 @@ struct Plan {
   ddp_status step(cudaStream_t s) {
     if (done >= nsteps) return fail(DDP_ERR_STATE, "all steps of this schedule are already enqueued");
     const int st = done;
+    DDP_NVTX_I(op == DDP_OP_BROADCAST ? "broadcast step"
+               : (op == DDP_OP_ALLGATHER || (op == DDP_OP_ALLREDUCE && st >= p - 1 && p > 1)) ? "all-gather step"
+                                                                                             : "reduce-scatter step",
+               st);
     const int es = (op == DDP_OP_BROADCAST) ? 1 : esize(dt);
     ddp_status rc = DDP_OK;
     if (op == DDP_OP_ALLREDUCE) {

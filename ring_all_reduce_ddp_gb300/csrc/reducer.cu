@@ -242,6 +242,7 @@ ddp_status reducer_sync_impl(ddp_reducer* h, float divisor, float predivide, ddp
   }
   const int es = esize(h->dt);
   for (auto& B : h->buckets) {
+    DDP_NVTX_I("bucket", static_cast<int>(&B - h->buckets.data()));
     const int32_t m = static_cast<int32_t>(B.members.size());
     SegBatcher sb(h->dt, predivide, stream);
     for (int32_t r = 0; r < p; ++r)
@@ -455,6 +456,7 @@ ddp_status ddp_reducer_mark_ready(ddp_reducer* h, int32_t tensor, float divisor,
       DDP_CUDA(cudaStreamWaitEvent(comm_stream, ready, 0), "wait on the gradient's ready event");
       waited = true;
     }
+    DDP_NVTX_I("bucket", h->next_bucket);
     DDP_TRY(run_bucket_launches(h->buckets[h->next_bucket].launches, h->dt, divisor, comm_stream, h->comm_blocks));
     ++h->next_bucket;
     ++n;

@@ -73,7 +73,8 @@ def test_error_text_is_per_thread():
 @pytest.mark.gpu
 def test_two_reducers_synced_from_two_threads_at_once():
     """Each thread owns a Reducer and a stream; both sync repeatedly at the
-    same time. The bits equal a sync of the same inputs run alone."""
+    same time. The bits equal the oracle's and a sync of the same inputs run
+    alone."""
     torch = pytest.importorskip("torch")
     from ring_all_reduce_ddp_gb300.reducer import Reducer
     from synth import workloads as W
@@ -112,6 +113,9 @@ def test_two_reducers_synced_from_two_threads_at_once():
         return run
 
     _run_threads([once(0), once(1)])
+    from tests.oracle_sync import check_whole_set
+    for g, red in zip(fresh, reds2):  # every element against the oracle
+        check_whole_set(cfg, red, g)
     for g in fresh:
         for r in range(cfg["p"]):
             for t in range(len(g[r])):
