@@ -186,3 +186,41 @@ def test_step_buffers_survive_a_rebuild():
     _, offset, bnumel = ob.bucket_layout(W.numels(cfg), plan)
     check_whole_set(cfg, red, grads, plan=(plan, offset, bnumel))
     _check_buffers(bufs, 1)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_step_buffers_misaligned_differently_per_replica(dtype):
+    """Buffers whose replicas sit at different addresses mod 16 bytes: their
+    copy tiles take the element-by-element path. The sizes leave ragged heads
+    and tails around the 16-byte words."""
+    cfg = dict(W.CONFIGS["tiny"], dtype=dtype)
+    p = cfg["p"]
+    grads, _ = W.make_grads(cfg)
+    red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+    esz = 4 if dtype == "f32" else 2
+    sizes = [1, 5, 1023, 1025, 4097]  # elements of the gradients' dtype
+    keep, rows, hosts = [], [], []
+    for r in range(p):
+        row, hrow = [], []
+        for j, n in enumerate(sizes):
+            shift = (r + j) % 4  # elements off the allocation's start: a different offset mod 16 per replica
+            raw = torch.zeros((n + 8) * esz, dtype=torch.uint8, device="cuda")
+            h = np.frombuffer(synth.values_np("uniform", 77, 900 + 10 * r + j, np.arange(n + 4)).tobytes(),
+                              dtype=np.uint8)[:n * esz].copy()
+            raw[shift * esz:(shift + n) * esz].copy_(torch.from_numpy(h))
+            keep.append(raw)
+            row.append(raw[shift * esz:(shift + n) * esz].view(TDT[dtype]))
+            hrow.append(h)
+        rows.append(row)
+        hosts.append(hrow)
+    root = 2
+    red.set_buffers(rows, root)
+    red.step(W.divisor(cfg))
+    torch.cuda.synchronize()
+    check_whole_set(cfg, red, grads)
+    want, _ = orc.broadcast_coalesced(hosts, root)
+    for r in range(p):
+        for j, t in enumerate(rows[r]):
+            got = t.view(torch.uint8).cpu().numpy()
+            assert np.array_equal(got, want[r][j]), (r, j)
+    assert D.ddp_device_error() == 0
