@@ -388,8 +388,9 @@ ddp_status ddp_reducer_step(ddp_reducer* handle, float divisor, cudaStream_t str
  * ddp_reducer_prepare resets the pending counts and the observed order.
  * ddp_reducer_mark_ready marks gradient `tensor` (registration index) ready:
  *   if that completes bucket next_bucket_ (and the ones after it), each of
- *   them is all-reduced in place (ddp_bucket_allreduce with divisor) on
- *   comm_stream, which first waits on `ready` (if not NULL: the event after
+ *   them is all-reduced in place (ddp_bucket_allreduce with divisor; the grid
+ *   as ddp_reducer_set_comm_blocks set it) on comm_stream, which first waits
+ *   on `ready` (if not NULL: the event after
  *   which the gradient holds its final value; events must complete in marking
  *   order, e.g. all recorded on one producing stream). *fired (if not NULL)
  *   = number of buckets launched by this call. DDP_ERR_STATE if the tensor was
