@@ -142,6 +142,7 @@ struct StagedArgs {
 constexpr int kBucketPtrs = 1024;
 constexpr int kBucketPieces = 256;
 constexpr int kBucketTileBytes = 4096;
+constexpr int kBucketThreads = kBucketTileBytes / 16;  // one 16-byte vector per thread and replica
 __host__ __device__ constexpr int64_t bucket_tile_elems(int elem_size) { return kBucketTileBytes / elem_size; }
 struct BucketArgs {
   void* ptr[kBucketPtrs];

@@ -199,7 +199,7 @@ __device__ __forceinline__ void bucket_tiles(const View& v, float divisor) {
 
 // Arguments by value (one bucket, from ddp_bucket_allreduce).
 template <typename T, int P>
-__global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_constant__ BucketArgs a) {
+__global__ void __launch_bounds__(kBucketThreads) k_bucket_allreduce(const __grid_constant__ BucketArgs a) {
   pdl_trigger();
   const View v{a.ptr, a.start, a.len, a.slot, a.origin, a.tile0, a.npieces, a.p};
   bucket_tiles<T, P>(v, a.divisor);
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce(const __grid_cons
 
 // Piece table in device memory (every bucket of a Reducer in one launch).
 template <typename T, int P>
-__global__ void __launch_bounds__(kThreads) k_bucket_allreduce_table(const BucketTable t, float divisor) {
+__global__ void __launch_bounds__(kBucketThreads) k_bucket_allreduce_table(const BucketTable t, float divisor) {
   pdl_trigger();
   const View v{t.ptr, t.start, t.len, t.slot, t.origin, t.tile0, t.npieces, t.p};
   bucket_tiles<T, P>(v, divisor);
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads) k_bucket_allreduce_table(const Bucke
 template <typename T>
 cudaError_t by_value(const BucketArgs& a, cudaStream_t s, int32_t max_blocks) {
   const int32_t tiles = a.tile0[a.npieces];
-  const dim3 grid(max_blocks > 0 ? std::min(tiles, max_blocks) : tiles), block(kThreads);
+  const dim3 grid(max_blocks > 0 ? std::min(tiles, max_blocks) : tiles), block(kBucketThreads);
   cudaError_t e;
   switch (a.p) {
     case 2: e = launch_pdl(k_bucket_allreduce<T, 2>, grid, block, 0, s, a); break;
@@ -244,7 +244,7 @@ template <typename T, int P>
 cudaError_t launch_table(const BucketTable& t, int32_t tiles, float divisor, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kBucketThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
