@@ -134,14 +134,17 @@ struct StagedArgs {
 // summation origin (its chunk index). ptr[slot * p + r] is replica r's tensor
 // in local slot `slot`; piece i covers elements [start, start + len) of that
 // tensor; tile0 is the prefix of each piece's tiles of bucket_tile_elems
-// elements. A tile is 4 KB per replica: one 16-byte vector per thread of a
-// 256-thread block, one block per tile. Measured on GB300 that way on the
-// ResNet-50-shaped set: 4, 8, 16, 32 and 64 KB tiles took 244.4, 246.6,
-// 250.4, 259.4 and 264.1 us; on the bf16 Llama-1B set 4 KB beat 8 and 64 KB
-// (5,499, 5,517 and 5,677 us).
+// elements. A tile is 2 KB per replica: one 16-byte vector per thread of a
+// 128-thread block, one block per tile. Measured on GB300 that way on the
+// ResNet-50-shaped set, with a binary piece search: 4, 8, 16, 32 and 64 KB
+// tiles took 244.4, 246.6, 250.4, 259.4 and 264.1 us; on the bf16 Llama-1B
+// set 4 KB beat 8 and 64 KB (5,499, 5,517 and 5,677 us). With the warps'
+// 32-way piece search, 2, 4 and 8 KB took 238.8-239.0, 239.0-239.9 and
+// 247.4-248.1 us on ResNet-50, 1,135-1,136, 1,136-1,138 and 1,159-1,167 us
+// on GPT-2, and 5,443-5,444, 5,454-5,455 and 5,843-5,846 us on Llama-1B.
 constexpr int kBucketPtrs = 1024;
 constexpr int kBucketPieces = 256;
-constexpr int kBucketTileBytes = 4096;
+constexpr int kBucketTileBytes = 2048;
 constexpr int kBucketThreads = kBucketTileBytes / 16;  // one 16-byte vector per thread and replica
 __host__ __device__ constexpr int64_t bucket_tile_elems(int elem_size) { return kBucketTileBytes / elem_size; }
 struct BucketArgs {
