@@ -277,13 +277,14 @@ def test_bucket_allreduce_in_place_matches_flatten_path_oracle(p, dtype, skew):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("p", [2, 3, 16, 17, 64])
+@pytest.mark.parametrize("p", [2, 3, 16, 17, 64, 256])
 def test_in_place_sync_every_replica_count_branch(p, dtype):
     """The whole-Reducer in-place sync (one launch over the device-resident
     piece table) at replica counts that take each of its compiled forms: p = 2
-    and 16 unrolled, 3, 17 and 64 the generic loop (p = 4 and 8 run in the
-    tests above). The tiny set's ten tensors on p replicas, every element
-    against the oracle's flatten + ring + unflatten on the oracle's own plan."""
+    and 16 unrolled, 3, 17, 64 and 256 (the largest the library takes) the
+    generic loop (p = 4 and 8 run in the tests above). The tiny set's ten
+    tensors on p replicas, every element against the oracle's flatten + ring +
+    unflatten on the oracle's own plan."""
     cfg = dict(W.CONFIGS["tiny"], dtype=dtype, p=p)
     grads, _ = W.make_grads(cfg, p=p)
     red = Reducer(grads, cfg["first_cap"], cfg["cap"])

@@ -71,7 +71,7 @@ def _check_buffers(bufs, root):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("p", [1, 2, 3, 4, 8, 16, 17])
+@pytest.mark.parametrize("p", [1, 2, 3, 4, 8, 16, 17, 256])
 def test_step_on_the_tiny_set_with_buffers(p, dtype):
     cfg = dict(W.CONFIGS["tiny"], dtype=dtype, p=p)
     grads, _ = W.make_grads(cfg, p=p)
