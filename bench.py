@@ -99,7 +99,6 @@ class Ranks:
 
     def barrier(self):
         if self.dist is not None:
-            import torch
             if self.backend == "nccl":
                 self.dist.barrier(device_ids=[self.local])
             else:
