@@ -22,10 +22,10 @@ pytestmark = pytest.mark.gpu
 
 GUARD = 4096
 SENTINEL = 0x5A
-# (dtype, elements): BatchNorm-like running stats and counters, odd sizes, a
-# few that span several 4 KB tiles
+# (dtype, elements): BatchNorm-like running stats and counters, odd sizes, an
+# empty one, a few that span several tiles
 BUFFER_SPECS = [("f32", 64), ("f32", 64), ("i64", 1), ("f32", 1), ("f32", 3), ("i64", 5), ("f32", 1000),
-                ("f32", 5000), ("i64", 2049), ("f32", 70001)]
+                ("f32", 0), ("f32", 5000), ("i64", 2049), ("f32", 70001)]
 BF16_EXTRA = [("bf16", 3), ("bf16", 1), ("bf16", 4099)]  # 2-byte multiples, for bf16 gradient sets
 TDT = {"f32": torch.float32, "i64": torch.int64, "bf16": torch.bfloat16}
 ESZ = {"f32": 4, "i64": 8, "bf16": 2}
