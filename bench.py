@@ -946,8 +946,8 @@ def run_overlap(args, ranks: Ranks):
     all-reduce on a communication stream. A step ends when the compute stream
     has waited for the communication stream (the optimizer needs the reduced
     gradients). For each cap, comm-stream priority and grid cap of the bucket
-    launches (0: one block per 4 KB tile; N > 0: N blocks striding over the
-    tiles, so the all-reduces hold at most about N/4 SMs at p = 8): the backward alone,
+    launches (0: one block per 2 KB tile; N > 0: N blocks striding over the
+    tiles, so the all-reduces hold at most about N/9 SMs at p = 8): the backward alone,
     backward + overlapped sync (with the time the compute stream took inside
     it), and backward followed by the sync. One JSON line per point."""
     import torch
@@ -1049,7 +1049,9 @@ def run_overlap(args, ranks: Ranks):
                 exposed = t_ov - t_bwd
                 print(json.dumps({"overlap": args.config, "p": cfg["p"], "bucket_cap_mb": cap / (1 << 20),
                                   "comm_stream_priority": prio, "comm_blocks": nblk,
-                                  "comm_sm_equivalent": round(nblk / 4, 1) if nblk else None,  # 4 blocks per SM at p = 8
+                                  # 9 blocks of the per-bucket kernel fit on an SM at p = 8 fp32
+                                  # (56 registers x 128 threads)
+                                  "comm_sm_equivalent": round(nblk / 9, 1) if nblk else None,
                                   "buckets": len(red.buckets), "n_tok": n_tok,
                                   "backward_ms": round(t_bwd, 4),
                                   "backward_tflops": round(flops / (t_bwd / 1e3) / 1e12, 1),
