@@ -407,7 +407,7 @@ ddp_status ddp_reducer_step(ddp_reducer* handle, float divisor, cudaStream_t str
  *   until a rebuild succeeds; destroy works as always. */
 ddp_status ddp_reducer_prepare(ddp_reducer* handle);
 /* The grid of the bucket launches ddp_reducer_mark_ready fires: max_blocks
- * == 0 (the default) gives one block per 4 KB tile; max_blocks > 0 at most
+ * == 0 (the default) gives one block per 2 KB tile; max_blocks > 0 at most
  * that many blocks, each striding over the bucket's tiles, as a collective
  * library bounds its kernels to a few channels. A bounded grid holds at most
  * max_blocks / (blocks resident per SM) SMs, so a backward pass running on
