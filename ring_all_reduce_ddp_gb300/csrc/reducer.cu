@@ -161,7 +161,7 @@ ddp_status build_reducer_table(ddp_reducer* h) {
 
 // (Re)build buckets from a walk order over the tensors: the flat-bucket
 // arenas, the bf16 workspace, each bucket's own in-place launches and the
-// whole-set piece table. Frees whatever device memory a previous build held.
+// whole-set piece table. Frees whatever device memory an earlier call held.
 ddp_status reducer_build(ddp_reducer* h, const std::vector<int32_t>& walk, bool reverse_list) {
   const int p = h->p, k = h->k, es = esize(h->dt);
   auto lists = walk_buckets(walk, h->numel.data(), es, h->first_cap, h->cap);
