@@ -363,7 +363,9 @@ ddp_status ddp_reducer_destroy(ddp_reducer* handle);
  *   for the device. If that allocation fails (DDP_ERR_NOMEM), no buffers stay
  *   attached and the reducer refuses sync, step, prepare and mark_ready
  *   (DDP_ERR_STATE) until a ddp_reducer_rebuild succeeds. k == 0 detaches.
- *   The buffers stay attached across ddp_reducer_rebuild.
+ *   A null handle, k < 0, root outside [0, p), null arrays with k > 0 or a
+ *   null buffer of nonzero size: DDP_ERR_ARG, and nothing changes. The
+ *   buffers stay attached across ddp_reducer_rebuild.
  * ddp_reducer_step enqueues on `stream` one launch that does both: the
  *   attached buffers copied from root to every other replica (the bits of
  *   ddp_broadcast_coalesced; the root's buffers are read, not written) and
