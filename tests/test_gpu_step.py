@@ -224,3 +224,40 @@ def test_step_buffers_misaligned_differently_per_replica(dtype):
             got = t.view(torch.uint8).cpu().numpy()
             assert np.array_equal(got, want[r][j]), (r, j)
     assert D.ddp_device_error() == 0
+
+
+def test_step_with_empty_gradients_and_a_tiny_cap():
+    """Zero-size gradient tensors (no storage) among others, a cap that
+    closes a bucket after every tensor, p = 3: the in-place sync and the
+    one-launch step skip the empty tensors and reduce the rest like the
+    oracle."""
+    p = 3
+    sizes = [0, 5, 0, 1000, 0, 4097, 1]
+    grads, hosts = [], []
+    for r in range(p):
+        row, hrow = [], []
+        for j, n in enumerate(sizes):
+            h = synth.values_np("normal", 3300, 10 * r + j, np.arange(n))
+            row.append(torch.from_numpy(h.copy()).cuda())
+            hrow.append(h)
+        grads.append(row)
+        hosts.append(hrow)
+    red = Reducer(grads, 4, 4)  # every non-empty tensor closes its bucket
+    bufs = _buffers(p, BUFFER_SPECS[:4], seed=95)
+    red.set_buffers([[b.t for b in row] for row in bufs], 0)
+    red.step(float(p))
+    torch.cuda.synchronize()
+    from oracle import buckets as ob
+    plan = ob.assign_buckets(sizes, 4, 4, 4)
+    assert red.buckets == plan
+    _, offset, bnumel = ob.bucket_layout(sizes, plan)
+    for b, members in enumerate(plan):
+        ins = [ob.flatten(hosts[r], members, offset, bnumel[b]) for r in range(p)]
+        want, _ = orc.allreduce(ins, bnumel[b], float(p))
+        for r in range(p):
+            back = ob.unflatten(want[r], members, offset, sizes)
+            for t in members:
+                got = grads[r][t].cpu().numpy()
+                assert np.array_equal(got.view(np.uint32), back[t].view(np.uint32)), (b, t, r)
+    _check_buffers(bufs, 0)
+    assert D.ddp_device_error() == 0
