@@ -49,3 +49,23 @@ def test_single_process_needs_no_group(monkeypatch):
     assert r.world == 1 and r.max(3.0) == 3.0
     r.barrier()
     r.close()
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
+    """`bench.py --impl reference` launched by torchrun with two ranks: rank 0
+    alone times the oracle and prints the JSON line; the other rank exits 0
+    without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, DDP_BENCH_BACKEND="gloo", OMP_NUM_THREADS="1")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1", "--config", "tiny"]
+    r = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
