@@ -70,3 +70,26 @@ def test_gpu_arm_line():
     assert all(x["gbs"] > 0 and abs(x["frac"] - x["gbs"] / r["peak"]) < 1e-3 for x in pts)
     assert set(d["configs"]) == {"gpt2_small", "llama_1b"}
     assert all(c["us"] > 0 and c["buckets_per_s"] > 0 for c in d["configs"].values())
+
+
+@pytest.mark.gpu
+def test_gpu_arm_under_torchrun_two_ranks():
+    """The N > 1 launch the contract uses (torchrun, one process per GPU),
+    here two gloo ranks sharing this machine's GPUs: one JSON line from rank
+    0, the whole-job value over both ranks, max-over-ranks timing."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    env = dict(os.environ, DDP_BENCH_BACKEND="gloo", OMP_NUM_THREADS="1")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           "bench.py", "--gpus", "2", "--steps", "5", "--warmup", "3", "--no-cpu-baseline"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    d = json.loads(lines[0])
+    _base(d)
+    assert d["n_gpus"] == 2 and d["value"] > 0 and d["gpu_launches"] == 5
+    assert "sweep" not in d and d["cpu_baseline"] is None
