@@ -12,6 +12,11 @@
 // same bits as the ring on the flat bucket. Work is cut into pieces (a tensor
 // intersected with a chunk: one origin each) and pieces into tiles of
 // bucket_tile_elems elements per replica; one block per tile.
+//
+// A Reducer's table may end with copy pieces, one per attached buffer: the
+// per-forward buffer broadcast ("PyTorch DDP Deep Dive", Part 2,
+// _sync_buffers -> _broadcast_coalesced) rides in the same launch as the
+// gradient sync (ddp_reducer_step).
 #include <algorithm>
 
 #include "launch.h"
