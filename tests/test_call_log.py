@@ -75,12 +75,17 @@ g = torch.cuda.CUDAGraph()
 with torch.cuda.graph(g):
     red.sync_gradients(W.divisor(cfg))
 torch.cuda.synchronize()
+bn = [[torch.zeros(10, device="cuda"), torch.zeros(3, dtype=torch.int64, device="cuda")] for _ in range(len(grads))]
+red.set_buffers(bn, root=1)
+red.step(W.divisor(cfg))
+torch.cuda.synchronize()
 """
     recs = _run(code, tmp_path / "log.jsonl")
     ops = [r["op"] for r in recs]
-    assert ops == ["ddp_allreduce", "ddp_allreduce", "ddp_reduce_scatter", "ddp_reducer_sync", "ddp_reducer_sync"]
+    assert ops == ["ddp_allreduce", "ddp_allreduce", "ddp_reduce_scatter", "ddp_reducer_sync", "ddp_reducer_sync",
+                   "ddp_reducer_step"]
     p, n, cs = 8, 1000003, -(-1000003 // 8)
-    ar, rd, rs, sync, captured = recs
+    ar, rd, rs, sync, captured, step = recs
     assert ar["bytes_algorithmic"] == 2 * p * n * 4 and ar["bytes_per_rank"] == 2 * (p - 1) * cs * 4
     assert rd["bytes_per_rank"] == 3 * n * 4  # log2 8 whole-buffer exchanges
     assert rs["bytes_algorithmic"] == (p + 1) * n * 4 and rs["bytes_per_rank"] == (p - 1) * cs * 4
@@ -88,3 +93,9 @@ torch.cuda.synchronize()
         assert r["status"] == "DDP_OK" and r["elapsed_us"] > 0
     assert sync["p"] == 4 and sync["n"] == 277421
     assert captured["elapsed_us"] is None  # inside a stream capture nothing is timed
+    # the step adds the broadcast of B = 10*4 + 3*8 bytes: p*B algorithmic,
+    # log2(p) copies of B per rank (the doubling tree's depth)
+    B = 10 * 4 + 3 * 8
+    assert step["status"] == "DDP_OK" and step["elapsed_us"] > 0 and step["n"] == sync["n"]
+    assert step["bytes_algorithmic"] == sync["bytes_algorithmic"] + 4 * B
+    assert step["bytes_per_rank"] == sync["bytes_per_rank"] + 2 * B
