@@ -405,8 +405,9 @@ def run_ours(args, ranks: Ranks):
     ms_per_step = ms_max / args.steps
     value = step_bytes * args.steps * ranks.world / (ms_max / 1e3) / 1e9
 
-    # Dominant kernel: the one-launch step (k_bucket_allreduce_table over the
-    # gradient pieces and the buffers' copy pieces). Its average duration is
+    # Dominant kernel: the one-launch step (the piece-table kernel, in the form
+    # ddp_reducer_staged names, over the gradient pieces and the buffers' copy
+    # pieces). Its average duration is
     # taken over ROOFLINE_LAUNCHES launches back to back on its stream, events
     # around the whole run: each launch reads the gradients the one before it
     # wrote, 0.8 GB at the default workload, more than L2 holds.
@@ -437,7 +438,9 @@ def run_ours(args, ranks: Ranks):
         traffic = int(NCU_TRAFFIC["dram_bytes_per_algorithmic_byte"] * kernel_bytes)
     bucket_mb = [round(n * esz / 2 ** 20, 2) for n in red.bucket_numel]
     nb = len(red.buckets)
-    kernel_name = ("k_bucket_allreduce_table: every bucket's flatten + ring-order all-reduce + unflatten and the "
+    table_kernel = ("k_bucket_table_staged (tiles staged in shared memory by bulk copies)" if red.staged()
+                    else "k_bucket_allreduce_table (register fold)")
+    kernel_name = (f"{table_kernel}: every bucket's flatten + ring-order all-reduce + unflatten and the "
                    "buffers' broadcast in one launch" if one_launch
                    else "flatten, fused all-reduce, unflatten per bucket (whole sync timed)")
 

@@ -333,6 +333,12 @@ ddp_status ddp_bucket_allreduce(int32_t p, int32_t k, void* const* grads, const 
  *   DDP_SYNC_IN_PLACE: every bucket's ddp_bucket_allreduce, all in ONE launch
  *     driven by a piece table uploaded to device memory at create (fused
  *     algos only; predivide must be 1). Tiles are ordered bucket by bucket.
+ *     DDP_ALGO_FUSED_TMA stages each 2 KB tile of every replica in shared
+ *     memory by bulk asynchronous copies before the fold (p = 2, 4, 8 or 16;
+ *     other p take the register form); a copy that does not complete within
+ *     2 s sets ddp_device_error() to 1 and leaves that tile unwritten.
+ *     DDP_ALGO_FUSED_LDST folds in registers; DDP_ALGO_FUSED takes the form
+ *     that ddp_reducer_staged reports.
  * Both give the same bits. */
 typedef struct ddp_reducer ddp_reducer;
 ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* const* grads,
@@ -340,6 +346,13 @@ ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* 
                               int64_t bucket_cap_bytes, ddp_border order);
 /* Number of buckets; -1 for a null handle. */
 int32_t ddp_reducer_num_buckets(const ddp_reducer* handle);
+/* 1 if this reducer's ddp_reducer_step and its in-place ddp_reducer_sync
+ * with DDP_ALGO_FUSED stage every tile in shared memory by bulk copies (the
+ * _FUSED_TMA form), 0 if they fold in registers (the _FUSED_LDST form); -1
+ * for a null handle. The choice depends only on the dtype and p: the form
+ * that measured faster on GB300 (staged for fp32 at p = 4 or 8 and for bf16
+ * at p = 2 or 4). Both give the same bits. */
+int32_t ddp_reducer_staged(const ddp_reducer* handle);
 /* Bucket b's element count and (if flat != NULL) its p flat buffers. */
 ddp_status ddp_reducer_bucket(const ddp_reducer* handle, int32_t b, int64_t* numel, void** flat);
 ddp_status ddp_reducer_sync(ddp_reducer* handle, float divisor, float predivide, ddp_algo algo,

@@ -56,6 +56,7 @@ _SIGS = {
     "ddp_bucket_allreduce": [_c_i32, _c_i32, _P_vp, _P_i64, _P_i64, _c_i32, _c_f32, _c_vp],
     "ddp_reducer_create": [ctypes.POINTER(_c_vp), _c_i32, _c_i32, _P_vp, _P_i64, _c_i32, _c_i64, _c_i64, _c_i32],
     "ddp_reducer_num_buckets": [_c_vp],
+    "ddp_reducer_staged": [_c_vp],
     "ddp_reducer_bucket": [_c_vp, _c_i32, _P_i64, _P_vp],
     "ddp_reducer_sync": [_c_vp, _c_f32, _c_f32, _c_i32, _c_i32, _c_vp],
     "ddp_reducer_destroy": [_c_vp],
@@ -85,7 +86,7 @@ _SIGS = {
     "ddp_last_error": [],
     "ddp_status_string": [_c_i32],
 }
-_RESTYPES = {"ddp_reducer_observed": _c_i32, "ddp_reducer_num_buckets": _c_i32, "ddp_ring_num_steps": _c_i32, "ddp_ring_steps_done": _c_i32, "ddp_kernel_launches": _c_i64,
+_RESTYPES = {"ddp_reducer_observed": _c_i32, "ddp_reducer_num_buckets": _c_i32, "ddp_reducer_staged": _c_i32, "ddp_ring_num_steps": _c_i32, "ddp_ring_steps_done": _c_i32, "ddp_kernel_launches": _c_i64,
              "ddp_last_error": ctypes.c_char_p, "ddp_status_string": ctypes.c_char_p}
 
 _lib = None
@@ -334,6 +335,10 @@ class DDPReducer:
 
     def num_buckets(self) -> int:
         return lib().ddp_reducer_num_buckets(self.h)
+
+    def staged(self) -> bool:
+        """True if step() and the default in-place sync take the shared-memory staged form."""
+        return lib().ddp_reducer_staged(self.h) == 1
 
     def bucket(self, b: int):
         """(element count, [p flat-buffer device pointers]) of bucket b."""

@@ -168,7 +168,12 @@ struct BucketTable {
   const int32_t* origin;
   const int32_t* tile0;  // npieces + 1 entries
   int npieces, p;
+  int* err;              // the library's device error word (the staged form's bounded waits), or null
 };
+
+// Codes of the library's device error word (ddp_device_error).
+constexpr int kErrBulkWait = 1;  // a bulk copy did not complete in time
+constexpr int kErrRingWait = 2;  // a ring step's wait ran out
 
 // Literal reduce-scatter step. x[r]: replica r's input (const except in the
 // fp32 in-place all-reduce); w: fp32 partials [2][p][cs]; out[d]: where the

@@ -18,7 +18,9 @@
 // _sync_buffers -> _broadcast_coalesced) rides in the same launch as the
 // gradient sync (ddp_reducer_step).
 #include <algorithm>
+#include <atomic>
 
+#include "bulk.cuh"
 #include "launch.h"
 
 namespace ddp {
@@ -218,6 +220,116 @@ __global__ void __launch_bounds__(kBucketThreads) k_bucket_allreduce_table(const
   bucket_tiles<T, P>(v, divisor);
 }
 
+// ------------------------------------------------------------ staged form
+// The same tiles with the loads staged through shared memory: lane j of warp
+// 0 issues a bulk asynchronous copy (cp.async.bulk, the TMA's non-tensor
+// form) of the tile's 16-byte-aligned body from replica j, all P completing
+// on one mbarrier; every thread then folds its 16 bytes from the P
+// staged copies in ring order and stores the result to every replica with
+// 128-bit stores. The few elements outside the aligned body (a tensor's
+// misaligned start or end) take the register form's plain loads while the
+// copies are in flight. The wait on the copies is bounded: past kStagedWaitNs
+// the block records kErrBulkWait in the device error word, waits once more
+// (bounded) for its copies to land, and stores nothing.
+constexpr int64_t kStagedWaitNs = 2000000000LL;
+
+template <typename T, int P>
+__global__ void __launch_bounds__(kBucketThreads) k_bucket_table_staged(const BucketTable t, float divisor) {
+  static_assert(P >= 2 && P * kBucketTileBytes <= 40 * 1024, "staged tiles of every replica must fit");
+  constexpr int V = Vec<T>::N;
+  constexpr int64_t kTile = bucket_tile_elems(sizeof(T));
+  __shared__ __align__(128) uint4 stage[P][kBucketThreads];  // replica (ring position) j's tile body
+  __shared__ __align__(8) uint64_t full;
+  __shared__ T* base[P];
+  pdl_trigger();
+  bool waited = false;
+  const View a{t.ptr, t.start, t.len, t.slot, t.origin, t.tile0, t.npieces, t.p};
+  const int32_t b = blockIdx.x;
+  if (b >= a.tile0[a.npieces]) {
+    wait_previous_grid(waited);
+    return;
+  }
+  const int i = find_piece(a.tile0, a.npieces, b);
+  const int64_t t0 = a.start[i] + static_cast<int64_t>(b - a.tile0[i]) * kTile;
+  const int64_t len = min(kTile, a.start[i] + a.len[i] - t0);
+  if (len <= 0) {
+    wait_previous_grid(waited);
+    return;
+  }
+  void* const* rep = a.ptr + static_cast<int64_t>(a.slot[i]) * P;
+  const int oi = a.origin[i];
+  const bool copy = oi >= P;  // a copy piece: replica oi - P's bits to the others
+  const int o = copy ? oi - P : oi;
+  const uint32_t bar = smem_addr(&full);
+  if (threadIdx.x < P) base[threadIdx.x] = reinterpret_cast<T*>(rep[(o + threadIdx.x) % P]);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  wait_previous_grid(waited);
+
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(base[0] + t0);
+  bool same = (a0 % sizeof(T)) == 0;
+  for (int r = 1; r < P && same; ++r) same = ((reinterpret_cast<uintptr_t>(base[r] + t0) ^ a0) & 15u) == 0;
+  int64_t head = len;
+  if (same) head = min(static_cast<int64_t>(((16u - (a0 & 15u)) & 15u) / sizeof(T)), len);
+  const int nvec = static_cast<int>((len - head) / V);
+  const int64_t tail0 = head + static_cast<int64_t>(nvec) * V;
+  const int loads = copy ? 1 : P;
+
+  if (threadIdx.x < 32 && nvec > 0) {  // warp 0: lane j copies replica j's body
+    const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, bytes * loads);
+    __syncwarp();
+    if (static_cast<int>(threadIdx.x) < loads)
+      bulk_load(smem_addr(stage[threadIdx.x]), base[threadIdx.x] + t0 + head, bytes, bar);
+  }
+
+  for (int64_t e = threadIdx.x; e < head + (len - tail0); e += blockDim.x) {
+    const int64_t x = t0 + (e < head ? e : tail0 + (e - head));
+    if (copy) {
+      const T y = base[0][x];
+      for (int q = 1; q < P; ++q) base[q][x] = y;
+      continue;
+    }
+    float acc = widen(base[0][x]);
+    for (int j = 1; j < P; ++j) acc = __fadd_rn(acc, widen(base[j][x]));
+    const T y = narrow<T>(__fdiv_rn(acc, divisor));
+    for (int q = 0; q < P; ++q) base[q][x] = y;
+  }
+  if (nvec == 0) return;
+
+  if (!mbar_wait_bounded(bar, 0, kStagedWaitNs)) {
+    if (t.err) atomicCAS(t.err, 0, kErrBulkWait);
+    (void)mbar_wait_bounded(bar, 0, kStagedWaitNs);  // the copies must land before shared memory goes away
+    return;
+  }
+  const int v = threadIdx.x;
+  if (v >= nvec) return;
+  const int64_t x = t0 + head + static_cast<int64_t>(v) * V;
+  if (copy) {
+    const uint4 y = stage[0][v];
+#pragma unroll
+    for (int q = 1; q < P; ++q) *reinterpret_cast<uint4*>(base[q] + x) = y;
+    return;
+  }
+  float acc[V];
+  Vec<T>::unpack(stage[0][v], acc);
+#pragma unroll
+  for (int j = 1; j < P; ++j) {
+    float u[V];
+    Vec<T>::unpack(stage[j][v], u);
+#pragma unroll
+    for (int l = 0; l < V; ++l) acc[l] = __fadd_rn(acc[l], u[l]);
+  }
+#pragma unroll
+  for (int l = 0; l < V; ++l) acc[l] = __fdiv_rn(acc[l], divisor);
+  const uint4 y = Vec<T>::pack(acc);
+#pragma unroll
+  for (int q = 0; q < P; ++q) *reinterpret_cast<uint4*>(base[q] + x) = y;
+}
+
 // One block per tile: blocks are dispatched in index order, so the resident
 // ones work on consecutive tiles. Measured on GB300 and slower: a persistent
 // grid striding over the tiles, and one taking tiles in order from a device
@@ -246,7 +358,23 @@ cudaError_t by_value(const BucketArgs& a, cudaStream_t s, int32_t max_blocks) {
 // Measured on GB300 on the ResNet-50-shaped step (buffer broadcast, then this
 // kernel): 263.1 -> 259.6 us per step.
 template <typename T, int P>
-cudaError_t launch_table(const BucketTable& t, int32_t tiles, float divisor, cudaStream_t s) {
+cudaError_t launch_table(const BucketTable& t, int32_t tiles, float divisor, cudaStream_t s, bool staged = false) {
+  if constexpr (P >= 2) {
+    if (staged) {
+      // as much shared memory as the SM has, so that the staged tiles rather
+      // than the L1 split limit the blocks per SM (set once per device)
+      static std::atomic<bool> configured[64];
+      int dev = 0;
+      cudaGetDevice(&dev);
+      if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
+        const cudaError_t e = cudaFuncSetAttribute(k_bucket_table_staged<T, P>,
+                                                   cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                   cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
+      }
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles);
   cfg.blockDim = dim3(kBucketThreads);
@@ -257,17 +385,22 @@ cudaError_t launch_table(const BucketTable& t, int32_t tiles, float divisor, cud
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if constexpr (P >= 2) {
+    if (staged) return cudaLaunchKernelEx(&cfg, k_bucket_table_staged<T, P>, t, divisor);
+  }
   return cudaLaunchKernelEx(&cfg, k_bucket_allreduce_table<T, P>, t, divisor);
 }
 
+// staged: the shared-memory staged form for p = 2, 4, 8 and 16; any other p
+// takes the register form.
 template <typename T>
-cudaError_t by_table(const BucketTable& t, int32_t tiles, float divisor, cudaStream_t s) {
+cudaError_t by_table(const BucketTable& t, int32_t tiles, float divisor, cudaStream_t s, bool staged) {
   cudaError_t e;
   switch (t.p) {
-    case 2: e = launch_table<T, 2>(t, tiles, divisor, s); break;
-    case 4: e = launch_table<T, 4>(t, tiles, divisor, s); break;
-    case 8: e = launch_table<T, 8>(t, tiles, divisor, s); break;
-    case 16: e = launch_table<T, 16>(t, tiles, divisor, s); break;
+    case 2: e = launch_table<T, 2>(t, tiles, divisor, s, staged); break;
+    case 4: e = launch_table<T, 4>(t, tiles, divisor, s, staged); break;
+    case 8: e = launch_table<T, 8>(t, tiles, divisor, s, staged); break;
+    case 16: e = launch_table<T, 16>(t, tiles, divisor, s, staged); break;
     default: e = launch_table<T, 0>(t, tiles, divisor, s); break;
   }
   count_launch();
@@ -281,11 +414,31 @@ cudaError_t launch_bucket_allreduce(const BucketArgs& a, ddp_dtype dt, cudaStrea
   return dt == DDP_FLOAT32 ? by_value<float>(a, s, max_blocks) : by_value<__nv_bfloat16>(a, s, max_blocks);
 }
 
+// Which form DDP_ALGO_FUSED takes: the staged one where it measured faster
+// on GB300 than the register one. In-place sync, launches back to back, best
+// of four, staged against registers:
+//   ResNet-50-shaped set (25.6 M gradients), fp32, p = 2, 4, 8, 16:
+//     70.7 / 120.2 / 236.2 / 480.9 us against 67.3 / 120.6 / 237.7 / 474.6;
+//   GPT-2-shaped set (124 M), fp32, p = 2, 4, 16: 321.9 / 566.1 / 2,303
+//     against 295.5 / 567.5 / 2,278 us (p = 8: 1,135.4 against 1,137.0);
+//   Llama-1B-shaped set (1.2 B), bf16, p = 2, 4, 8: 1,661 / 2,746 / 5,475
+//     against 1,724 / 2,777 / 5,460 us.
+// (The ResNet-50-shaped set in bf16 also favoured the staged form at p = 2
+// and 4, 38.0 / 62.4 against 41.7 / 70.0 us, but partly from L2.) The
+// one-launch step on the ResNet-50-shaped set, with its 159 buffers: 236.9
+// against 238.8 us. At p = 16 the staged tiles (32 KB a block) leave room for
+// six blocks per SM; at p = 2 a tile is too little work to repay the mbarrier
+// round trip.
+bool staged_by_default(ddp_dtype dt, int p) {
+  return dt == DDP_FLOAT32 ? (p == 4 || p == 8) : (p == 2 || p == 4);
+}
+
 cudaError_t launch_bucket_table(const BucketTable& t, int32_t total_tiles, float divisor, ddp_dtype dt,
-                                cudaStream_t s) {
+                                cudaStream_t s, ddp_algo algo) {
   if (t.npieces <= 0 || total_tiles <= 0) return cudaSuccess;
-  return dt == DDP_FLOAT32 ? by_table<float>(t, total_tiles, divisor, s)
-                           : by_table<__nv_bfloat16>(t, total_tiles, divisor, s);
+  const bool staged = algo == DDP_ALGO_FUSED_TMA || (algo == DDP_ALGO_FUSED && staged_by_default(dt, t.p));
+  return dt == DDP_FLOAT32 ? by_table<float>(t, total_tiles, divisor, s, staged)
+                           : by_table<__nv_bfloat16>(t, total_tiles, divisor, s, staged);
 }
 
 }  // namespace ddp

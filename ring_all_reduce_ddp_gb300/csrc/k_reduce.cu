@@ -198,7 +198,6 @@ __global__ void __launch_bounds__(kFusedThreads) k_fused_reduce_ldst(const __gri
 // thread writes that tile back to every replica with p bulk stores. Stages are
 // recycled in a ring so several tiles are in flight per SM.
 constexpr int kMaxStages = 8;
-constexpr int kErrBulkWait = 1;  // device error code: a bulk copy did not complete in time
 
 template <typename T>
 __device__ __forceinline__ void staged_scalar(const StagedArgs& a, int c, int64_t i) {
@@ -504,7 +503,6 @@ __global__ void __launch_bounds__(kThreads) k_rs_step_ws(const __grid_constant__
 // st.release.gpu: the release is cumulative over the block's writes ordered
 // before it by the barrier, so no separate fence is needed (an extra
 // fence.acq_rel cost 7-12 % of the step time).
-constexpr int kErrRingWait = 2;  // device error code: a ring step's wait ran out
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
@@ -800,6 +798,11 @@ cudaError_t launch_ring_persistent(const PersistArgs& a, cudaStream_t s) {
                                                     dim3(a.p * a.blocks_per_rank), dim3(kThreads), args, 0, s);
   count_launch();
   return e;
+}
+
+int* device_error_word() {
+  void* p = nullptr;
+  return cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess ? static_cast<int*>(p) : nullptr;
 }
 
 cudaError_t read_device_error(cudaStream_t s, int* code) {

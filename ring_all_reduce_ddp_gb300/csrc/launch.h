@@ -15,8 +15,12 @@ cudaError_t launch_rs_step_inplace_f32(const RingStepArgs& a, cudaStream_t s);
 cudaError_t launch_rs_step_ws(const RingStepArgs& a, ddp_dtype dt, cudaStream_t s);
 // max_blocks > 0 caps the grid: each block then strides over the tiles.
 cudaError_t launch_bucket_allreduce(const BucketArgs& a, ddp_dtype dt, cudaStream_t s, int32_t max_blocks = 0);
+// algo: DDP_ALGO_FUSED_LDST the register form, DDP_ALGO_FUSED_TMA the
+// shared-memory staged form (p = 2, 4, 8, 16; others take the register form),
+// DDP_ALGO_FUSED whichever measured faster for the dtype and p.
 cudaError_t launch_bucket_table(const BucketTable& t, int32_t total_tiles, float divisor, ddp_dtype dt,
-                                cudaStream_t s);
+                                cudaStream_t s, ddp_algo algo);
+bool staged_by_default(ddp_dtype dt, int p);  // the form DDP_ALGO_FUSED takes in launch_bucket_table
 cudaError_t launch_ring_persistent(const PersistArgs& a, cudaStream_t s);
 int ring_persistent_max_blocks();  // co-resident blocks of the persistent ring kernel on this device
 cudaError_t launch_pair_copy(const PairCopyArgs& a, cudaStream_t s);
@@ -26,6 +30,8 @@ cudaError_t launch_seg_copy(const SegCopyArgs& a, ddp_dtype dt, cudaStream_t s);
 cudaError_t launch_multi_fanout(const MultiFanoutArgs& a, cudaStream_t s);
 cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t s);
 
+// Device address of the library's device error word in the current context.
+int* device_error_word();
 // Synchronize s, then read and clear the device error word.
 cudaError_t read_device_error(cudaStream_t s, int* code);
 

@@ -153,6 +153,7 @@ ddp_status build_reducer_table(ddp_reducer* h) {
   h->table.tile0 = reinterpret_cast<const int32_t*>(d + o_tile0);
   h->table.npieces = static_cast<int>(np);
   h->table.p = p;
+  h->table.err = device_error_word();
   h->table_tiles = tile0.back();
   h->sync_pieces = sync_pieces;
   h->sync_tiles = sync_tiles;
@@ -237,7 +238,7 @@ ddp_status reducer_sync_impl(ddp_reducer* h, float divisor, float predivide, ddp
     DDP_CHECK(predivide == 1.0f, DDP_ERR_ARG, "the in-place sync has no pre-divide");
     BucketTable sync = h->table;  // the gradient pieces only: the copy pieces come after them
     sync.npieces = h->sync_pieces;
-    DDP_CUDA(launch_bucket_table(sync, h->sync_tiles, divisor, h->dt, stream), "in-place sync launch");
+    DDP_CUDA(launch_bucket_table(sync, h->sync_tiles, divisor, h->dt, stream, algo), "in-place sync launch");
     return DDP_OK;
   }
   const int es = esize(h->dt);
@@ -280,7 +281,8 @@ ddp_status reducer_step_impl(ddp_reducer* h, float divisor, cudaStream_t stream)
   DDP_CHECK(h != nullptr, DDP_ERR_ARG, "handle is null");
   DDP_TRY(check_divisor(divisor));
   DDP_CHECK(!h->unbuilt, DDP_ERR_STATE, "the reducer's last rebuild failed; rebuild it again or destroy it");
-  DDP_CUDA(launch_bucket_table(h->table, h->table_tiles, divisor, h->dt, stream), "reducer step launch");
+  DDP_CUDA(launch_bucket_table(h->table, h->table_tiles, divisor, h->dt, stream, DDP_ALGO_FUSED),
+           "reducer step launch");
   return DDP_OK;
 }
 
@@ -340,6 +342,8 @@ ddp_status ddp_reducer_create(ddp_reducer** handle, int32_t p, int32_t k, void* 
 }
 
 int32_t ddp_reducer_num_buckets(const ddp_reducer* h) { return h ? static_cast<int32_t>(h->buckets.size()) : -1; }
+
+int32_t ddp_reducer_staged(const ddp_reducer* h) { return h ? (ddp::staged_by_default(h->dt, h->p) ? 1 : 0) : -1; }
 
 ddp_status ddp_reducer_bucket(const ddp_reducer* h, int32_t b, int64_t* numel, void** flat) {
   DDP_CHECK(h && numel, DDP_ERR_ARG, "null argument");

@@ -95,6 +95,7 @@ int main() {
     CHECK(ddp_reducer_create(&h, p, k, grads.data(), numel, DDP_FLOAT32, 1024, 4096, DDP_ORDER_REVERSED) == DDP_OK,
           "ddp_reducer_create");
     CHECK(ddp_reducer_num_buckets(h) >= 1, "buckets");
+    CHECK(ddp_reducer_staged(h) == 0 && ddp_reducer_staged(nullptr) == -1, "ddp_reducer_staged");  // fp32, p = 2: registers
     CHECK(ddp_reducer_sync(h, 2.0f, 1.0f, DDP_ALGO_FUSED, DDP_SYNC_IN_PLACE, s) == DDP_OK, "ddp_reducer_sync");
     CHECK(cudaStreamSynchronize(s) == cudaSuccess, "sync");
     for (int r = 0; r < p; ++r)

@@ -94,6 +94,7 @@ def test_argument_errors_are_reported_before_any_launch(L):
     assert lib.ddp_broadcast(arr, 2, 16, 5, 0, None) == L.DDP_ERR_ARG                # root out of range
     # zero-size work is a no-op that touches no device
     assert lib.ddp_allreduce(arr, 2, 0, 0, 1.0, 0, None) == L.DDP_OK
+    assert lib.ddp_reducer_num_buckets(None) == -1 and lib.ddp_reducer_staged(None) == -1
 
 
 @pytest.mark.parametrize("seed", range(20))

@@ -176,8 +176,9 @@ def test_broadcast_handle_tree_steps(p, root):
 
 
 # ------------------------------------------------------------- whole syncs
-SYNCS = [(D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE), (D.DDP_ALGO_FUSED, D.DDP_SYNC_FLATTEN),
-         (D.DDP_ALGO_FUSED_TMA, D.DDP_SYNC_FLATTEN), (D.DDP_ALGO_RING_STEPS, D.DDP_SYNC_FLATTEN)]
+SYNCS = [(D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE), (D.DDP_ALGO_FUSED_TMA, D.DDP_SYNC_IN_PLACE),
+         (D.DDP_ALGO_FUSED, D.DDP_SYNC_FLATTEN), (D.DDP_ALGO_FUSED_TMA, D.DDP_SYNC_FLATTEN),
+         (D.DDP_ALGO_RING_STEPS, D.DDP_SYNC_FLATTEN)]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -276,32 +277,49 @@ def test_bucket_allreduce_in_place_matches_flatten_path_oracle(p, dtype, skew):
     assert D.ddp_device_error() == 0
 
 
+@pytest.mark.parametrize("algo", [D.DDP_ALGO_FUSED, D.DDP_ALGO_FUSED_TMA])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("p", [2, 3, 16, 17, 64, 256])
-def test_in_place_sync_every_replica_count_branch(p, dtype):
+def test_in_place_sync_every_replica_count_branch(p, dtype, algo):
     """The whole-Reducer in-place sync (one launch over the device-resident
     piece table) at replica counts that take each of its compiled forms: p = 2
-    and 16 unrolled, 3, 17, 64 and 256 (the largest the library takes) the
-    generic loop (p = 4 and 8 run in the tests above). The tiny set's ten
-    tensors on p replicas, every element against the oracle's flatten + ring +
-    unflatten on the oracle's own plan."""
+    and 16 unrolled (register or shared-memory staged), 3, 17, 64 and 256 (the
+    largest the library takes) the generic register loop (p = 4 and 8 run in
+    the tests above). The tiny set's ten tensors on p replicas, every element
+    against the oracle's flatten + ring + unflatten on the oracle's own plan."""
     cfg = dict(W.CONFIGS["tiny"], dtype=dtype, p=p)
     grads, _ = W.make_grads(cfg, p=p)
     red = Reducer(grads, cfg["first_cap"], cfg["cap"])
-    red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE)
+    red.sync_gradients(W.divisor(cfg), algo, D.DDP_SYNC_IN_PLACE)
     torch.cuda.synchronize()
     check_whole_set(cfg, red, grads)
     assert D.ddp_device_error() == 0
 
 
-@pytest.mark.parametrize("mode", [D.DDP_SYNC_IN_PLACE, D.DDP_SYNC_FLATTEN])
+def test_default_in_place_form_per_dtype_and_replica_count():
+    """ddp_reducer_staged reports the form DDP_ALGO_FUSED takes in place:
+    staged for fp32 at p = 4 and 8 and for bf16 at p = 2 and 4, registers
+    elsewhere (the header's table)."""
+    want = {("f32", 4), ("f32", 8), ("bf16", 2), ("bf16", 4)}
+    for dtype in ("f32", "bf16"):
+        for p in (1, 2, 3, 4, 8, 16, 17):
+            cfg = dict(W.CONFIGS["tiny"], dtype=dtype, p=p)
+            grads, _ = W.make_grads_from_host(cfg, p=p)
+            red = Reducer(grads, cfg["first_cap"], cfg["cap"])
+            assert red.staged() == ((dtype, p) in want), (dtype, p)
+            red.destroy()
+
+
+@pytest.mark.parametrize("algo,mode", [(D.DDP_ALGO_FUSED, D.DDP_SYNC_IN_PLACE),
+                                       (D.DDP_ALGO_FUSED_TMA, D.DDP_SYNC_IN_PLACE),
+                                       (D.DDP_ALGO_FUSED, D.DDP_SYNC_FLATTEN)])
 @pytest.mark.parametrize("name", ["resnet50", "gpt2_small"])
-def test_model_sized_sync_sampled_parity(name, mode):
+def test_model_sized_sync_sampled_parity(name, algo, mode):
     """Full-size fp32 gradient sets in the bench's launch configuration."""
     cfg = W.CONFIGS[name]
     grads, _ = W.make_grads(cfg)
     red = Reducer(grads, cfg["first_cap"], cfg["cap"])
-    red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED, mode)
+    red.sync_gradients(W.divisor(cfg), algo, mode)
     torch.cuda.synchronize()
     check_sync_sampled(cfg, red, grads, np.random.default_rng(5))
     # every replica ends identical (the data-parallel invariant), on whole tensors
@@ -311,13 +329,14 @@ def test_model_sized_sync_sampled_parity(name, mode):
     assert D.ddp_device_error() == 0
 
 
-@pytest.mark.parametrize("one_launch", [False, True])
-def test_llama_bf16_sync_and_buffer_broadcast_sampled_parity(one_launch):
+@pytest.mark.parametrize("one_launch,algo", [(False, D.DDP_ALGO_FUSED), (False, D.DDP_ALGO_FUSED_TMA),
+                                             (True, None)])
+def test_llama_bf16_sync_and_buffer_broadcast_sampled_parity(one_launch, algo):
     """1.2B bf16 gradients on 8 replicas (about 39 GB with the buckets), and the
     per-forward broadcast of 64 fp32 buffers from replica 0: as two calls (the
-    coalesced broadcast, then the in-place sync) and as the one-launch step
-    the bench's configs field times. Buffers against the oracle's coalesced
-    broadcast of the host-generated bytes."""
+    coalesced broadcast, then the in-place sync, register or staged form) and
+    as the one-launch step the bench's configs field times. Buffers against
+    the oracle's coalesced broadcast of the host-generated bytes."""
     cfg = W.CONFIGS["llama_1b"]
     bufs = W.buffer_set(cfg)
     host = W.buffer_set_host(cfg)
@@ -330,7 +349,7 @@ def test_llama_bf16_sync_and_buffer_broadcast_sampled_parity(one_launch):
         red.step(W.divisor(cfg))
     else:
         broadcast_buffers(bufs, 0)
-        red.sync_gradients(W.divisor(cfg), D.DDP_ALGO_FUSED)
+        red.sync_gradients(W.divisor(cfg), algo)
     torch.cuda.synchronize()
     for r in range(cfg["p"]):
         for j, b in enumerate(bufs[r]):
