@@ -26,11 +26,14 @@ NS = list(range(0, 71))
 class Guarded:
     """n elements of dtype in the middle of a sentinel-filled allocation."""
 
-    def __init__(self, n, dtype, r=0, seed=0, kind="normal", fill=True):
+    def __init__(self, n, dtype, r=0, seed=0, kind="normal", fill=True, shift=0):
+        """shift: elements between the margin and the tensor, so that the
+        tensor's start can sit off a 16-byte boundary."""
         self.esz = 4 if dtype == "f32" else 2
         self.tdt = torch.float32 if dtype == "f32" else torch.bfloat16
-        self.g = GUARD // self.esz
-        self.raw = torch.full((2 * GUARD + max(n, 1) * self.esz,), SENTINEL, dtype=torch.uint8, device="cuda")
+        self.g = GUARD // self.esz + shift
+        self.raw = torch.full((2 * GUARD + (max(n, 1) + shift) * self.esz,), SENTINEL, dtype=torch.uint8,
+                              device="cuda")
         self.t = self.raw.view(self.tdt)[self.g:self.g + n]
         self.n = n
         if fill and n:
@@ -38,8 +41,9 @@ class Guarded:
 
     def margins_intact(self):
         raw = self.raw.cpu().numpy()
-        end = GUARD + self.n * self.esz
-        return bool((raw[:GUARD] == SENTINEL).all() and (raw[end:] == SENTINEL).all())
+        lo = self.g * self.esz
+        end = lo + self.n * self.esz
+        return bool((raw[:lo] == SENTINEL).all() and (raw[end:] == SENTINEL).all())
 
 
 def _host(g, dtype):
@@ -161,6 +165,70 @@ def test_in_place_bucket_small_tensors_stay_inside():
                 for j in range(k):
                     assert gs[r][j].margins_intact(), (p, case, r, j)
                     assert _eq(_host(gs[r][j], "f32"), back[j]), (p, case, r, j)
+
+
+@pytest.mark.parametrize("form", ["register", "staged", "step"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_reducer_table_forms_stay_inside(dtype, form):
+    """The Reducer's one-launch piece-table kernel, register form
+    (DDP_ALGO_FUSED_LDST), staged form (DDP_ALGO_FUSED_TMA) and the default
+    one-launch step with attached buffers, at p = 2, 3, 4, 8 and 16: tensors
+    of 0..1,299 elements (up to three 2 KB tiles), each in its own guarded
+    allocation, starting 0-3 elements off a 16-byte boundary by the same
+    amount on every replica (the staged form's bulk copies) or, in every
+    other case, by an amount that differs between replicas (the scalar path).
+    Small caps give several buckets. Margins intact, gradients equal to the
+    oracle's flatten + ring + unflatten on the oracle's own plan, buffers
+    equal to the root's bytes."""
+    from oracle import buckets as ob
+    from oracle.bf16 import bf16_to_f32, f32_to_bf16
+    from ring_all_reduce_ddp_gb300.reducer import Reducer
+    esz = 4 if dtype == "f32" else 2
+    rng = np.random.default_rng(13 if dtype == "f32" else 14)
+    algo = {"register": D.DDP_ALGO_FUSED_LDST, "staged": D.DDP_ALGO_FUSED_TMA, "step": None}[form]
+    for p in (2, 3, 4, 8, 16):
+        for case in range(4):
+            k = int(rng.integers(1, 9))
+            sizes = [int(x) for x in rng.integers(0, 1300, size=k)]
+            skew = case % 2 == 1
+            shift = [[(3 * t + (r if skew else 0)) % 4 for t in range(k)] for r in range(p)]
+            gs = [[Guarded(sz, dtype, r * 10 + t, 1300 + case, shift=shift[r][t]) for t, sz in enumerate(sizes)]
+                  for r in range(p)]
+            hosts = [[_host(g, dtype) for g in row] for row in gs]
+            first, cap = 1024, 4096
+            red = Reducer([[g.t for g in row] for row in gs], first, cap)
+            plan = ob.assign_buckets(sizes, esz, first, cap, "reversed")
+            _, offset, bnumel = ob.bucket_layout(sizes, plan)
+            assert red.buckets == plan
+            bufs = None
+            if form == "step":
+                bsizes = [int(x) for x in rng.integers(0, 700, size=3)]
+                bufs = [[Guarded(sz, "f32", r * 10 + j, 1400 + case, kind="uniform", shift=(j + r) % 4)
+                         for j, sz in enumerate(bsizes)] for r in range(p)]
+                want_b = [_host(g, "f32") for g in bufs[p - 1]]
+                red.set_buffers([[g.t for g in row] for row in bufs], p - 1)
+                red.step(float(p))
+            else:
+                red.sync_gradients(float(p), algo, D.DDP_SYNC_IN_PLACE)
+            torch.cuda.synchronize()
+            for b, members in enumerate(plan):
+                wide = [[bf16_to_f32(h) if dtype == "bf16" else h for h in hosts[r]] for r in range(p)]
+                ins = [ob.flatten(wide[r], members, offset, bnumel[b]) for r in range(p)]
+                if dtype == "bf16":
+                    ins = [f32_to_bf16(x) for x in ins]
+                want, _ = orc.allreduce(ins, bnumel[b], float(p), dtype)
+                for r in range(p):
+                    back = ob.unflatten(want[r], members, offset, sizes)
+                    for t in members:
+                        assert gs[r][t].margins_intact(), (p, case, r, t)
+                        assert _eq(_host(gs[r][t], dtype), back[t]), (p, case, r, t)
+            if bufs is not None:
+                for r in range(p):
+                    for j, g in enumerate(bufs[r]):
+                        assert g.margins_intact(), (p, case, r, j)
+                        assert _eq(_host(g, "f32"), want_b[j]), (p, case, r, j)
+            red.destroy()
+            assert D.ddp_device_error() == 0
 
 
 def test_persistent_ring_small_sizes_stay_inside():

@@ -87,3 +87,39 @@ def test_in_place_bucket_keeps_subnormals(p):
         for t in members:
             assert_bit_equal(to_host(grads[r][t]), back[t], f"tensor {t} replica {r}")
     assert D.ddp_device_error() == 0
+
+
+@pytest.mark.parametrize("algo", [D.DDP_ALGO_FUSED_LDST, D.DDP_ALGO_FUSED_TMA])
+@pytest.mark.parametrize("p", [2, 4, 8, 16])
+def test_reducer_table_forms_keep_subnormals(p, algo):
+    """The whole-Reducer in-place sync, register and shared-memory staged
+    forms, on three tensors whose values sit in the subnormal range."""
+    from ring_all_reduce_ddp_gb300.reducer import Reducer
+    sizes = [1000, 37, 5001]
+    n = sum(sizes)
+    flat_hosts = _tiny_values(p, n, 3300 + p)
+    grads, hosts = [], []
+    for r in range(p):
+        row, hrow, pos = [], [], 0
+        for sz in sizes:
+            h = flat_hosts[r][pos:pos + sz].copy()
+            row.append(torch.from_numpy(h).cuda())
+            hrow.append(h)
+            pos += sz
+        grads.append(row)
+        hosts.append(hrow)
+    red = Reducer(grads, 1 << 20, 25 << 20)
+    plan = ob.assign_buckets(sizes, 4, 1 << 20, 25 << 20, "reversed")
+    _, offset, bnumel = ob.bucket_layout(sizes, plan)
+    assert red.buckets == plan == [[2, 1, 0]]
+    red.sync_gradients(float(p), algo, D.DDP_SYNC_IN_PLACE)
+    torch.cuda.synchronize()
+    members = plan[0]
+    ins = [ob.flatten(hosts[r], members, offset, bnumel[0]) for r in range(p)]
+    want, _ = orc.allreduce(ins, bnumel[0], float(p))
+    for r in range(p):
+        back = ob.unflatten(want[r], members, offset, sizes)
+        for t in members:
+            assert_bit_equal(to_host(grads[r][t]), back[t], f"tensor {t} replica {r}")
+    red.destroy()
+    assert D.ddp_device_error() == 0
