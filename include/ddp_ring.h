@@ -100,8 +100,9 @@ typedef enum {
   DDP_ALGO_RING_STEPS = 1,  /* the literal schedule: one launch per ring step         */
   DDP_ALGO_FUSED_LDST = 2,  /* one pass through registers (128-bit loads and stores) */
   DDP_ALGO_FUSED_TMA = 3,   /* one pass staged through shared memory by bulk
-                               asynchronous copies (falls back to the register path
-                               when p > 16 or the replicas' alignments differ)      */
+                               asynchronous copies, p = 2, 4, 8 or 16 (any other p,
+                               replicas at different addresses mod 16, or the
+                               per-hop bf16 flag take the register path)            */
   /* Tree-shaped literal all-reduces ([DP] "Latency, trees, and choosing an
    * algorithm"; [COLL] tree all-reduce). ddp_allreduce only; the pairwise
    * tree order, not the ring's. bf16 buffers are widened into a stream-ordered
@@ -511,7 +512,10 @@ ddp_status ddp_ring_destroy(ddp_ring* handle);
 
 /* Synchronize `stream`, then read and clear the library's device error word:
  * *code = 0 when no kernel reported a problem, else the first code a kernel
- * recorded (a bounded wait that gave up). Returns DDP_ERR_TIMEOUT if set. */
+ * recorded (a bounded wait that gave up): 1 a bulk copy of a shared-memory
+ * staged kernel (DDP_ALGO_FUSED_TMA, or a staged in-place sync or step) did
+ * not complete within 2 s, and that block stored nothing; 2 a persistent
+ * ring step's wait ran out. Returns DDP_ERR_TIMEOUT if set. */
 ddp_status ddp_device_error(cudaStream_t stream, int32_t* code);
 /* Number of kernels this library has launched in this process. */
 int64_t ddp_kernel_launches(void);

@@ -110,24 +110,6 @@ struct FusedArgs {
   int hop_round;     // bf16 only: round each partial to bf16 after every add
 };
 
-// Fused reduction staged through shared memory by bulk (TMA) copies. Chunk c's
-// 16-byte-aligned body [body_lo[c], body_lo[c] + body_len[c]) is cut into tiles
-// of tile_elems; tile0 is the prefix of tiles over chunks. The few elements of
-// a chunk outside its body take the scalar path.
-constexpr int kMaxStagedP = 64;
-struct StagedArgs {
-  void* rep[kMaxStagedP];      // the p input replicas (the all-reduce's outputs too)
-  void* out[kMaxStagedP];      // reduce-scatter: out[rank]
-  int64_t body_lo[kMaxStagedP];
-  int64_t body_len[kMaxStagedP];
-  int32_t tile0[kMaxStagedP + 1];
-  int64_t n, cs;
-  float divisor;
-  int p, scatter, shift;
-  int stages, tile_elems;
-  int64_t timeout_ns;          // bound of every wait on a bulk copy
-};
-
 // Bucket all-reduce straight on the gradients (flatten + all-reduce +
 // unflatten in one pass). A bucket's virtual flat layout is cut into pieces:
 // the intersections of its tensors with its chunks, so each piece has one

@@ -191,182 +191,118 @@ __global__ void __launch_bounds__(kFusedThreads) k_fused_reduce_ldst(const __gri
 }
 
 
-// ------------------------------------ fused, staged through shared memory
-// Bulk asynchronous copies (the TMA's non-tensor form): one elected thread
-// loads a tile of every replica into shared memory and signals an mbarrier;
-// all threads fold the p copies in ring order into a result tile; the elected
-// thread writes that tile back to every replica with p bulk stores. Stages are
-// recycled in a ring so several tiles are in flight per SM.
-constexpr int kMaxStages = 8;
+// ------------------------------- fused, one-shot staging through shared memory
+// The register kernel's grid (one block of 128 threads per window of 128 * U
+// vectors of a chunk, in index order), with the loads staged: lane j of warp
+// 0 issues one bulk asynchronous copy (cp.async.bulk) of replica j's window,
+// all P completing on one mbarrier; each thread then folds its U vectors from
+// shared memory in ring order and stores with 128-bit stores. No pipeline and
+// no hand-off between warps: the many resident blocks keep the copies in
+// flight. A block loops over further windows only when the grid had to be
+// capped. Every wait is bounded; the block decides together (a barrier vote)
+// whether its copies landed, and on a timeout records kErrBulkWait, waits
+// once more (bounded) for the copies and stops.
+constexpr int64_t kBulkWaitNs = 2000000000LL;  // bound of every wait on a bulk copy
 
-template <typename T>
-__device__ __forceinline__ void staged_scalar(const StagedArgs& a, int c, int64_t i) {
-  const int p = a.p;
-  const int o = (c + a.shift) % p;
-  float acc = widen(reinterpret_cast<const T*>(a.rep[o])[i]);
-  int r = o;
-  for (int j = 1; j < p; ++j) {
-    r = (r + 1 == p) ? 0 : r + 1;
-    acc = __fadd_rn(acc, widen(reinterpret_cast<const T*>(a.rep[r])[i]));
-  }
-  const T y = narrow<T>(__fdiv_rn(acc, a.divisor));
-  if (a.scatter) {
-    reinterpret_cast<T*>(a.out[(o + p - 1) % p])[i - static_cast<int64_t>(c) * a.cs] = y;
-  } else {
-    for (int q = 0; q < p; ++q) reinterpret_cast<T*>(a.rep[q])[i] = y;
-  }
-}
-
-// Sixteen consumer warps and tiles sized for about three stages: measured on
-// GB300 against 8 warps and 4-8 smaller stages, this took the staged
-// all-reduce from 0.89 to 0.94 of measured HBM at p = 8 and from 0.39 to 0.96
-// at p = 64 (reduce-scatter: 0.74 -> 1.03 and 0.20 -> 1.04).
-constexpr int kConsumerWarps = 16;
-constexpr int kStagedThreads = 32 * (1 + kConsumerWarps);  // warp 0 produces, warps 1.. consume
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Warp-specialised pipeline over S stages of p tile slots each.
-//   producer (warp 0, one lane): for its j-th tile, waits until stage j % S
-//     is released, then loads the p replicas' tiles into it with bulk copies
-//     that complete on full[st];
-//   consumers (warps 1..16): wait on full[st]; each thread folds its vectors of
-//     the p slots in ring order in registers, divides, and writes the result
-//     with 128-bit stores straight to every replica (or to the scatter
-//     output); then each warp arrives on empty[st], and the stage is released
-//     once all sixteen have read it.
-// Only loads go through shared memory: the TMA engine keeps a whole stage per
-// replica in flight for one issuing thread, and no consumer barrier or
-// store-completion wait sits between tiles. Every wait is bounded; on a
-// timeout the CTA records the error and stops.
-template <typename T>
-__global__ void __launch_bounds__(kStagedThreads, 1) k_fused_reduce_staged(const __grid_constant__ StagedArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
+template <typename T, int P>
+__global__ void __launch_bounds__(kFusedThreads) k_fused_reduce_oneshot(const __grid_constant__ FusedArgs a) {
+  constexpr int U = ldst_unroll<P>();
+  constexpr int W = kFusedThreads * U;  // vectors per window
   constexpr int V = Vec<T>::N;
-  const int p = a.p;
-  const int S = a.stages;
-  const int tile_bytes = a.tile_elems * static_cast<int>(sizeof(T));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kMaxStages;
-  unsigned char* data = smem + 128;  // [S][p][tile_bytes]
-  __shared__ int s_abort;
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  const int ctid = threadIdx.x - 32;  // consumer thread index (valid for warp >= 1)
-
-  // 1. elements outside the aligned bodies: consumers, chunks round-robin over CTAs
-  if (warp >= 1) {
-    for (int c = blockIdx.x; c < p; c += gridDim.x) {
-      const int64_t lo = min(a.n, static_cast<int64_t>(c) * a.cs);
-      const int64_t hi = min(a.n, lo + a.cs);
-      const int64_t b0 = a.body_lo[c], b1 = a.body_lo[c] + a.body_len[c];
-      for (int64_t i = lo + ctid; i < b0; i += 32 * kConsumerWarps) staged_scalar<T>(a, c, i);
-      for (int64_t i = b1 + ctid; i < hi; i += 32 * kConsumerWarps) staged_scalar<T>(a, c, i);
+  __shared__ __align__(128) uint4 stage[P][W];
+  __shared__ __align__(8) uint64_t full;
+  __shared__ T* dst[P];
+  pdl_trigger();
+  pdl_wait();
+  const int c = blockIdx.y;
+  const int64_t lo = static_cast<int64_t>(c) * a.cs;
+  const int64_t hi = min(a.n, lo + a.cs);
+  if (lo >= hi) return;
+  const int o = (c + a.shift) % P;
+  const int owner = (o + P - 1) % P;
+  const T* const* src = reinterpret_cast<const T* const*>(&a.src[o]);
+  T* sdst = a.scatter ? reinterpret_cast<T*>(a.dst[owner]) : nullptr;
+  const int64_t len = hi - lo;
+  int64_t head = len;
+  if (a.same_align) {
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(src[0] + lo);
+    const int64_t h = static_cast<int64_t>(((16u - (addr & 15u)) & 15u) / sizeof(T));
+    bool ok = (addr % sizeof(T)) == 0;
+    if (a.scatter) ok = ok && ((reinterpret_cast<uintptr_t>(sdst + h) & 15u) == 0);
+    if (ok) head = min(h, len);
+  }
+  const int64_t nvec = (len - head) / V;
+  const int64_t tail0 = head + nvec * V;
+  const int64_t nscalar = head + (len - tail0);
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t gstride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // The few elements outside the aligned body, one loaded value at a time
+  // (not unrolled: P values in flight here would set the register count of
+  // the whole kernel, 80 instead of 44 at p = 16).
+  for (int64_t e = gtid; e < nscalar; e += gstride) {
+    const int64_t i = lo + (e < head ? e : tail0 + (e - head));
+    float acc = widen(src[0][i]);
+#pragma unroll 1
+    for (int j = 1; j < P; ++j) acc = __fadd_rn(acc, widen(src[j][i]));
+    const T y = narrow<T>(__fdiv_rn(acc, a.divisor));
+    if (a.scatter) {
+      sdst[i - lo] = y;
+    } else {
+#pragma unroll 1
+      for (int r = 0; r < P; ++r) reinterpret_cast<T*>(a.dst[r])[i] = y;
     }
   }
-
-  const int32_t total = a.tile0[p];
-  const int my_tiles = (static_cast<int32_t>(blockIdx.x) < total)
-                           ? (total - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                           : 0;
-  if (my_tiles == 0) return;
+  int64_t v0 = static_cast<int64_t>(blockIdx.x) * W;
+  if (v0 >= nvec) return;
+  const uint32_t bar = smem_addr(&full);
   if (threadIdx.x == 0) {
-    s_abort = 0;
-    for (int st = 0; st < S; ++st) {
-      mbar_init(smem_addr(&full[st]), 1);
-      mbar_init(smem_addr(&empty[st]), kConsumerWarps);
-    }
+    mbar_init(bar, 1);
     fence_mbar_init();
   }
+  // the destinations in shared memory, read as each store needs them, rather
+  // than P pointers held in registers across the loop
+  if (threadIdx.x < P) dst[threadIdx.x] = reinterpret_cast<T*>(a.dst[threadIdx.x]);
   __syncthreads();
-
-  auto tile_at = [&](int j, int& c, int64_t& i0, int& len) {
-    const int32_t g = static_cast<int32_t>(blockIdx.x) + j * static_cast<int32_t>(gridDim.x);
-    int lo = 0, hi = p;  // tile0[lo] <= g < tile0[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (a.tile0[mid] <= g) lo = mid; else hi = mid;
+  for (uint32_t phase = 0; v0 < nvec; v0 += static_cast<int64_t>(gridDim.x) * W, phase ^= 1u) {
+    const int cnt = static_cast<int>(min(static_cast<int64_t>(W), nvec - v0));
+    if (threadIdx.x < 32) {
+      const uint32_t bytes = static_cast<uint32_t>(cnt) * 16u;
+      if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, bytes * P);
+      __syncwarp();
+      if (static_cast<int>(threadIdx.x) < P)
+        bulk_load(smem_addr(stage[threadIdx.x]), src[threadIdx.x] + lo + head + v0 * V, bytes, bar);
     }
-    c = lo;
-    const int64_t off = static_cast<int64_t>(g - a.tile0[c]) * a.tile_elems;
-    i0 = a.body_lo[c] + off;
-    len = static_cast<int>(min(static_cast<int64_t>(a.tile_elems), a.body_len[c] - off));
-  };
-
-  if (warp == 0) {
-    if (lane == 0) {
-      int j = 0;
-      for (; j < my_tiles; ++j) {
-        const int st = j % S;
-        if (j >= S) {
-          const uint32_t parity = static_cast<uint32_t>(j / S - 1) & 1u;
-          if (!mbar_wait_bounded(smem_addr(&empty[st]), parity, a.timeout_ns)) {
-            atomicCAS(&g_device_error, 0, kErrBulkWait);
-            atomicExch(&s_abort, 1);
-            break;
-          }
-        }
-        if (atomicAdd(&s_abort, 0)) break;
-        int c, len;
-        int64_t i0;
-        tile_at(j, c, i0, len);
-        const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
-        const uint32_t bar = smem_addr(&full[st]);
-        mbar_arrive_expect_tx(bar, bytes * p);
-        for (int r = 0; r < p; ++r)
-          bulk_load(smem_addr(data + (static_cast<size_t>(st) * p + r) * tile_bytes),
-                    reinterpret_cast<const T*>(a.rep[r]) + i0, bytes, bar);
-      }
-      // the loads issued for tiles the consumers will never take (after an
-      // abort) must land before the CTA's shared memory goes away
-      for (int k = j - S; k < j; ++k)
-        if (k >= 0) (void)mbar_wait_bounded(smem_addr(&full[k % S]), static_cast<uint32_t>(k / S) & 1u, a.timeout_ns);
+    const bool landed = mbar_wait_bounded(bar, phase, kBulkWaitNs);
+    if (!__syncthreads_and(landed)) {
+      if (threadIdx.x == 0) atomicCAS(&g_device_error, 0, kErrBulkWait);
+      (void)mbar_wait_bounded(bar, phase, kBulkWaitNs);  // the copies must land before shared memory goes away
+      return;
     }
-    return;
-  }
-
-  // consumers
-  for (int j = 0; j < my_tiles; ++j) {
-    const int st = j % S;
-    const uint32_t parity = static_cast<uint32_t>(j / S) & 1u;
-    if (!mbar_wait_bounded(smem_addr(&full[st]), parity, a.timeout_ns)) {
-      atomicCAS(&g_device_error, 0, kErrBulkWait);
-      atomicExch(&s_abort, 1);
-      break;
-    }
-    int c, len;
-    int64_t i0;
-    tile_at(j, c, i0, len);
-    const int o = (c + a.shift) % p;
-    const unsigned char* stage = data + static_cast<size_t>(st) * p * tile_bytes;
-    const int nvec = len / V;
-    for (int v = ctid; v < nvec; v += 32 * kConsumerWarps) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = threadIdx.x + u * kFusedThreads;
+      if (v >= cnt) break;
       float acc[V];
-      Vec<T>::unpack(*reinterpret_cast<const uint4*>(stage + static_cast<size_t>(o) * tile_bytes + v * 16), acc);
-      int r = o;
-      for (int q = 1; q < p; ++q) {
-        r = (r + 1 == p) ? 0 : r + 1;
+      Vec<T>::unpack(stage[0][v], acc);
+#pragma unroll 1
+      for (int j = 1; j < P; ++j) {  // one staged vector at a time: shared memory is close, registers are not free
         float t[V];
-        Vec<T>::unpack(*reinterpret_cast<const uint4*>(stage + static_cast<size_t>(r) * tile_bytes + v * 16), t);
+        Vec<T>::unpack(stage[j][v], t);
 #pragma unroll
         for (int l = 0; l < V; ++l) acc[l] = __fadd_rn(acc[l], t[l]);
       }
 #pragma unroll
       for (int l = 0; l < V; ++l) acc[l] = __fdiv_rn(acc[l], a.divisor);
       const uint4 y = Vec<T>::pack(acc);
-      const int64_t x = i0 + static_cast<int64_t>(v) * V;
+      const int64_t i = lo + head + (v0 + v) * V;
       if (a.scatter) {
-        T* d = reinterpret_cast<T*>(a.out[(o + p - 1) % p]) + (x - static_cast<int64_t>(c) * a.cs);
-        *reinterpret_cast<uint4*>(d) = y;
+        *reinterpret_cast<uint4*>(sdst + (i - lo)) = y;
       } else {
-        for (int q = 0; q < p; ++q) *reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.rep[q]) + x) = y;
+#pragma unroll
+        for (int r = 0; r < P; ++r) *reinterpret_cast<uint4*>(dst[r] + i) = y;
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
-    if (atomicAdd(&s_abort, 0)) break;
+    __syncthreads();  // every thread is done with this window before the next one's copies land
   }
 }
 
@@ -687,84 +623,45 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 int64_t launches() { return g_launches.load(std::memory_order_relaxed); }
 
 namespace {
-constexpr int kStagedSmemBudget = 220 * 1024;
-constexpr int kStagedBestP = 16;
-
-// Plan the staged kernel; false when its conditions do not hold (more than
-// kStagedBestP replicas, replicas not sharing an alignment, a scatter output
-// that is not 16-byte aligned where its chunk's body starts).
-template <typename T>
-bool plan_staged(const FusedArgs& f, StagedArgs& a) {
+template <typename T, int P>
+cudaError_t launch_oneshot(const FusedArgs& a, cudaStream_t s) {
   constexpr int V = Vec<T>::N;
-  const int p = f.p;
-  // Above 16 replicas the stages hold 1 KB tiles or less and the register
-  // path is faster (measured at p = 64: 0.77 against 0.95 of HBM).
-  if (p > kStagedBestP || !f.same_align || f.hop_round) return false;
-  const uintptr_t base = reinterpret_cast<uintptr_t>(f.src[0]);
-  if (base % sizeof(T) != 0) return false;
-  std::memset(&a, 0, sizeof(a));
-  int tile_bytes = 16384;
-  while (tile_bytes > 512 && static_cast<int64_t>(p) * tile_bytes * 2 > kStagedSmemBudget) tile_bytes /= 2;
-  int stages = static_cast<int>(kStagedSmemBudget / (static_cast<int64_t>(p) * tile_bytes));
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (stages < 2) return false;
-  a.tile_elems = tile_bytes / static_cast<int>(sizeof(T));
-  a.stages = stages;
-  a.n = f.n; a.cs = f.cs; a.divisor = f.divisor; a.p = p; a.scatter = f.scatter; a.shift = f.shift;
-  a.timeout_ns = 2000000000LL;
-  int64_t tiles = 0;
-  for (int c = 0; c < p; ++c) {
-    a.rep[c] = const_cast<void*>(f.src[c]);
-    a.out[c] = f.dst[c];
-  }
-  for (int c = 0; c < p; ++c) {
-    const int64_t lo = std::min(f.n, static_cast<int64_t>(c) * f.cs);
-    const int64_t hi = std::min(f.n, lo + f.cs);
-    const uintptr_t addr = base + static_cast<uintptr_t>(lo) * sizeof(T);
-    int64_t head = static_cast<int64_t>(((16u - (addr & 15u)) & 15u) / sizeof(T));
-    if (head > hi - lo) head = hi - lo;
-    const int64_t body = (hi - lo - head) / V * V;
-    a.body_lo[c] = lo + head;
-    a.body_len[c] = body;
-    if (f.scatter && body > 0) {
-      const int owner = ((c + f.shift) % p + p - 1) % p;
-      const uintptr_t d = reinterpret_cast<uintptr_t>(f.dst[owner]) + static_cast<uintptr_t>(head) * sizeof(T);
-      if (d & 15u) return false;
-    }
-    a.tile0[c] = static_cast<int32_t>(tiles);
-    tiles += (body + a.tile_elems - 1) / a.tile_elems;
-    if (tiles > 0x7FFFFFFF) return false;
-  }
-  a.tile0[p] = static_cast<int32_t>(tiles);
-  return true;
-}
-
-template <typename T>
-cudaError_t fused_staged(const StagedArgs& a, cudaStream_t s) {
-  const size_t smem = 128 + static_cast<size_t>(a.stages) * a.p * a.tile_elems * sizeof(T);
-  static std::atomic<bool> configured[64];  // per device; setting the attribute twice is harmless
+  constexpr int W = kFusedThreads * ldst_unroll<P>();
+  static std::atomic<bool> configured[64];  // shared memory as large as the SM allows, set once per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
-    const cudaError_t e = cudaFuncSetAttribute(k_fused_reduce_staged<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kStagedSmemBudget + 1024);
+    const cudaError_t e = cudaFuncSetAttribute(k_fused_reduce_oneshot<T, P>,
+                                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
-  int grid = sm_count();
-  if (a.tile0[a.p] < grid) grid = a.tile0[a.p] > a.p ? a.tile0[a.p] : a.p;
-  if (grid < 1) grid = 1;
-  k_fused_reduce_staged<T><<<grid, kStagedThreads, smem, s>>>(a);
+  const cudaError_t e = launch_pdl(k_fused_reduce_oneshot<T, P>,
+                                   dim3(fused_blocks_per_chunk(a.cs / V + 1, W), a.p), dim3(kFusedThreads), 0, s, a);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// The one-shot staged kernel for p = 2, 4, 8 and 16 with every replica at
+// the same address mod 16; false when it does not apply.
+template <typename T>
+bool oneshot(const FusedArgs& a, cudaStream_t s, cudaError_t* e) {
+  if (!a.same_align || a.hop_round) return false;
+  switch (a.p) {
+    case 2: *e = launch_oneshot<T, 2>(a, s); return true;
+    case 4: *e = launch_oneshot<T, 4>(a, s); return true;
+    case 8: *e = launch_oneshot<T, 8>(a, s); return true;
+    case 16: *e = launch_oneshot<T, 16>(a, s); return true;
+    default: return false;
+  }
 }
 }  // namespace
 
 cudaError_t launch_fused_reduce(const FusedArgs& a, ddp_dtype dt, bool staged, cudaStream_t s) {
   if (staged) {
-    StagedArgs sa;
-    if (dt == DDP_FLOAT32 ? plan_staged<float>(a, sa) : plan_staged<__nv_bfloat16>(a, sa))
-      return dt == DDP_FLOAT32 ? fused_staged<float>(sa, s) : fused_staged<__nv_bfloat16>(sa, s);
+    cudaError_t e = cudaSuccess;
+    if (dt == DDP_FLOAT32 ? oneshot<float>(a, s, &e) : oneshot<__nv_bfloat16>(a, s, &e)) return e;
   }
   if (dt == DDP_FLOAT32) return fused_ldst<float, false>(a, s);
   return a.hop_round ? fused_ldst<__nv_bfloat16, true>(a, s) : fused_ldst<__nv_bfloat16, false>(a, s);
