@@ -211,3 +211,44 @@ def test_comm_blocks_must_not_be_negative():
     with pytest.raises(D.DDPError) as e:
         red.set_comm_blocks(-1)
     assert e.value.status == D.DDP_ERR_ARG
+
+
+def test_first_use_of_the_staged_kernels_inside_a_capture():
+    """In a fresh process, the staged in-place sync and the staged flat
+    all-reduce are first launched inside a CUDA graph capture (they set no
+    function attribute and allocate nothing on first use); the replay gives
+    the eager bits."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = """
+import torch
+import ring_all_reduce_ddp_gb300 as D
+from ring_all_reduce_ddp_gb300.reducer import Reducer
+from synth import workloads as W
+cfg = dict(W.CONFIGS["tiny"], p=8)
+sets = [W.make_grads_from_host(cfg, p=8)[0] for _ in range(2)]
+reds = [Reducer(g, cfg["first_cap"], cfg["cap"]) for g in sets]
+assert reds[0].staged()
+n = (1 << 20) + 3
+flats = [[torch.arange(n, device="cuda", dtype=torch.float32) * (r + 1) / 7 for r in range(8)] for _ in range(2)]
+torch.cuda.synchronize()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g):
+    reds[0].sync_gradients(8.0)
+    D.ddp_allreduce(flats[0], n, D.DDP_FLOAT32, 8.0, D.DDP_ALGO_FUSED_TMA)
+g.replay()
+reds[1].sync_gradients(8.0)
+D.ddp_allreduce(flats[1], n, D.DDP_FLOAT32, 8.0, D.DDP_ALGO_FUSED_TMA)
+torch.cuda.synchronize()
+for r in range(8):
+    for a, b in zip(sets[0][r], sets[1][r]):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.equal(flats[0][r].view(torch.int32), flats[1][r].view(torch.int32))
+assert D.ddp_device_error() == 0
+print("ok")
+"""
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=300,
+                       env=dict(os.environ, PYTHONPATH=root))
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stderr[-2000:]
