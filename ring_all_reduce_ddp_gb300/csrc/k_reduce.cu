@@ -692,7 +692,9 @@ cudaError_t launch_ring_persistent(const PersistArgs& a, cudaStream_t s) {
 
 int* device_error_word() {
   void* p = nullptr;
-  return cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess ? static_cast<int*>(p) : nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) return static_cast<int*>(p);
+  (void)cudaGetLastError();  // leave no error behind for a later launch check to misreport
+  return nullptr;
 }
 
 cudaError_t read_device_error(cudaStream_t s, int* code) {
