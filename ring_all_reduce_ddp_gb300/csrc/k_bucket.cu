@@ -17,6 +17,12 @@
 // per-forward buffer broadcast ("PyTorch DDP Deep Dive", Part 2,
 // _sync_buffers -> _broadcast_coalesced) rides in the same launch as the
 // gradient sync (ddp_reducer_step).
+//
+// The whole-Reducer table kernel comes in two forms with the same bits: the
+// register fold (k_bucket_allreduce_table) and a form that stages each tile
+// in shared memory by bulk copies (k_bucket_table_staged); staged_by_default
+// says which one DDP_ALGO_FUSED and the step take. A single bucket's launch
+// (k_bucket_allreduce, table by value) always folds in registers.
 #include <algorithm>
 
 #include "bulk.cuh"
