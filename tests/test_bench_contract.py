@@ -61,6 +61,8 @@ def test_gpu_arm_line():
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0 < r["frac"] < 1.2 and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
     assert r["event_timed_launches"] >= 32
+    assert r["kernel"].startswith("k_bucket_table_staged")  # fp32 at p = 8 takes the staged form
+    assert r["traffic"] is None or 0.9 < r["traffic"] / r["algorithmic_bytes_per_launch"] < 1.05
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 20  # the buffer broadcast and the sync: one launch every step
