@@ -32,11 +32,26 @@ __device__ int g_device_error = 0;
 // from 64 MiB within 0.002 either way (p = 8, 1 GiB: 1.036 both).
 constexpr int kFusedThreads = 128;
 
-// Vectors per thread (U): with p = 2 or 4 a vector needs only two or four
-// loads, so on large chunks each thread takes four or two vectors and keeps
-// eight 16-byte loads in flight; larger p already does.
+// Vectors per thread (U): with few replicas a vector needs few loads, so on
+// large chunks a thread may take two vectors to keep more 16-byte loads in
+// flight. Measured on GB300, flat fp32, CUDA graph of launches after an L2
+// flush, fraction of measured HBM at 16 / 25 / 64 / 256 MiB:
+//   all-reduce p = 2, U = 2: 0.867 / 0.917 / 0.988 / 1.035; U = 4: 0.844 /
+//     0.904 / 0.981 / 1.029; U = 1: 0.724 / 0.772 / 0.818 / 0.845;
+//   all-reduce p = 4, U = 1: 0.935 / 0.974 / 1.014 / 1.036; U = 2: 0.935 /
+//     0.968 / 1.012 / 1.031;
+//   reduce-scatter p = 2, U = 2: 0.819 / 0.902 / 1.007 / 1.068; U = 4: 0.801
+//     / 0.888 / 0.990 / 1.047;
+//   reduce-scatter p = 4, U = 2: 0.918 / 0.975 / 1.050 / 1.073; U = 1: 0.834
+//     / 0.887 / 0.941 / 0.990 (it writes one output per p inputs, so its
+//     stores do not keep the memory system busy the way p stores do).
+// So U = 2 for p = 2, and for the reduce-scatter at p = 4; U = 1 otherwise.
+constexpr int ldst_unroll(int p, bool scatter) { return (p == 2 || (p == 4 && scatter)) ? 2 : 1; }
+
+// Vectors per thread of the one-shot staged kernel's window, as measured
+// with it (a 16 KB staging buffer per block at p = 2 and 4).
 template <int P>
-__host__ __device__ constexpr int ldst_unroll() { return P == 2 ? 4 : P == 4 ? 2 : 1; }
+__host__ __device__ constexpr int oneshot_unroll() { return P == 2 ? 4 : P == 4 ? 2 : 1; }
 
 template <typename T, int P, bool HOP = false, int U = 1>
 __global__ void __launch_bounds__(kFusedThreads) k_fused_reduce_ldst(const __grid_constant__ FusedArgs a) {
@@ -206,7 +221,7 @@ constexpr int64_t kBulkWaitNs = 2000000000LL;  // bound of every wait on a bulk 
 
 template <typename T, int P>
 __global__ void __launch_bounds__(kFusedThreads) k_fused_reduce_oneshot(const __grid_constant__ FusedArgs a) {
-  constexpr int U = ldst_unroll<P>();
+  constexpr int U = oneshot_unroll<P>();
   constexpr int W = kFusedThreads * U;  // vectors per window
   constexpr int V = Vec<T>::N;
   __shared__ __align__(128) uint4 stage[P][W];
@@ -579,12 +594,13 @@ int fused_blocks_per_chunk(int64_t vectors, int per_block) {
 template <typename T, int P, bool HOP>
 cudaError_t launch_ldst(const FusedArgs& a, cudaStream_t s) {
   constexpr int V = Vec<T>::N;
-  constexpr int UP = ldst_unroll<P>();
   const int64_t vectors = a.cs / V + 1;
-  if constexpr (UP > 1) {
-    const int bx = fused_blocks_per_chunk(vectors, kFusedThreads * UP);
-    if (static_cast<int64_t>(bx) * a.p >= 8 * static_cast<int64_t>(sm_count()))
-      return launch_pdl(k_fused_reduce_ldst<T, P, HOP, UP>, dim3(bx, a.p), dim3(kFusedThreads), 0, s, a);
+  if constexpr (P == 2 || P == 4) {
+    if (ldst_unroll(P, a.scatter != 0) == 2) {
+      const int bx = fused_blocks_per_chunk(vectors, kFusedThreads * 2);
+      if (static_cast<int64_t>(bx) * a.p >= 8 * static_cast<int64_t>(sm_count()))
+        return launch_pdl(k_fused_reduce_ldst<T, P, HOP, 2>, dim3(bx, a.p), dim3(kFusedThreads), 0, s, a);
+    }
   }
   return launch_pdl(k_fused_reduce_ldst<T, P, HOP, 1>, dim3(fused_blocks_per_chunk(vectors, kFusedThreads), a.p),
                     dim3(kFusedThreads), 0, s, a);
@@ -629,7 +645,7 @@ namespace {
 template <typename T, int P>
 cudaError_t launch_oneshot(const FusedArgs& a, cudaStream_t s) {
   constexpr int V = Vec<T>::N;
-  constexpr int W = kFusedThreads * ldst_unroll<P>();
+  constexpr int W = kFusedThreads * oneshot_unroll<P>();
   const cudaError_t e = launch_pdl(k_fused_reduce_oneshot<T, P>,
                                    dim3(fused_blocks_per_chunk(a.cs / V + 1, W), a.p), dim3(kFusedThreads), 0, s, a);
   count_launch();
