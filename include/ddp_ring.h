@@ -278,14 +278,20 @@ ddp_status ddp_reduce_scatter(const void* const* in, void* const* out, int32_t p
  *   in[p]:  m elements each: rank r's finished chunk, chunk r (DDP_OWN_RANK) or
  *           chunk (r+1) mod p (DDP_OWN_RING)
  *   out[p]: p*m elements each; every out[r] ends holding all chunks in order.
- * A copy: bit-exact, no scaling. out must not overlap in. */
+ * A copy: bit-exact, no scaling. out must not overlap in. The fused forms
+ * read each chunk once and write it p times: _FUSED_LDST through registers,
+ * _FUSED_TMA by bulk copies through shared memory (8 KB tiles; where a source
+ * and a destination differ modulo 16 bytes, registers), _FUSED the bulk
+ * copies with 7 or more destinations from 64 MiB read in all, else registers.
+ * Same fan-out for ddp_broadcast. */
 ddp_status ddp_allgather(const void* const* in, void* const* out, int32_t p, int64_t m,
                          ddp_dtype dtype, ddp_own own, ddp_algo algo, cudaStream_t stream);
 
 /* Broadcast nbytes from bufs[root] to every other replica. [COLL] code/main.py
  * list (broadcast over a doubling tree). RING_STEPS runs the tree: with
  * v = (r - root) mod p, at step j every v < 2^j copies to v + 2^j (< p);
- * ceil(log2 p) launches. FUSED reads the root once and writes p-1 copies. */
+ * ceil(log2 p) launches. FUSED reads the root once and writes p-1 copies
+ * (the fused forms as for ddp_allgather). */
 ddp_status ddp_broadcast(void* const* bufs, int32_t p, int64_t nbytes, int32_t root,
                          ddp_algo algo, cudaStream_t stream);
 

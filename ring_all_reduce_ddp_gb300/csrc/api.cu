@@ -170,7 +170,7 @@ ddp_status allgather_impl(const void* const* in, void* const* out, int32_t p, in
   a.nbytes = m * es;
   a.njobs = p;
   a.ndst = p;
-  DDP_CUDA(launch_fanout(a, stream), "all-gather launch");
+  DDP_CUDA(launch_fanout(a, stream, algo), "all-gather launch");
   return DDP_OK;
 }
 
@@ -201,7 +201,7 @@ ddp_status broadcast_impl(void* const* bufs, int32_t p, int64_t nbytes, int32_t 
   a.nbytes = nbytes;
   a.njobs = 1;
   a.ndst = q;
-  DDP_CUDA(launch_fanout(a, stream), "broadcast launch");
+  DDP_CUDA(launch_fanout(a, stream, algo), "broadcast launch");
   return DDP_OK;
 }
 

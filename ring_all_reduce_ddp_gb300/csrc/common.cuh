@@ -224,6 +224,7 @@ struct FanoutArgs {
   char* dst[kMaxP];
   int64_t nbytes;
   int njobs, ndst;
+  int* err;  // the library's device error word (the bulk-copy form's bounded waits), or null
 };
 
 // Segment copy (multi-tensor): segment s copies bytes[s] bytes from src[s] to

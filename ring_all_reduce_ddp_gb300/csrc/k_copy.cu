@@ -13,6 +13,7 @@
 // Every copy picks the widest word (16, 8, 4, 2 or 1 bytes) on which source
 // and destination agree modulo its size, copies the bytes before the first
 // boundary and after the last one singly, and the words in between.
+#include "bulk.cuh"
 #include "launch.h"
 
 namespace ddp {
@@ -108,6 +109,68 @@ __global__ void __launch_bounds__(kThreads) k_fanout(const __grid_constant__ Fan
     __syncthreads();
     copy_to_all<U>(a.src[j] + b0, dst, a.ndst, len, threadIdx.x, blockDim.x);
   }
+}
+
+// The fused fan-out with the TMA's bulk copies: each block is one warp with
+// one tile of the job's source. Lane 0 loads the tile into shared memory with
+// one bulk copy (completing on an mbarrier); then the lanes write it to the
+// destinations, one bulk store each, so the copy engine of the SM moves every
+// byte and no thread holds data in registers. Every source and destination
+// must agree modulo 16 bytes (the host checks); the bytes before the first
+// 16-byte boundary of the source and after the last one go singly. The wait
+// for the load is bounded: past kBulkFanWaitNs the block records kErrBulkWait,
+// waits once more (bounded) and stops. A block waits for its stores to
+// complete before it ends.
+// 8 KB tiles: measured on GB300 against 16 and 32 KB, broadcast and
+// all-gather at 64 MiB per replica, p = 8 / 16 / 64: 0.98 / 1.00 / 1.04 of
+// measured HBM against 0.96 / 0.96 / 1.00 (16 KB) and 0.97 / 0.95 / 0.96
+// (32 KB); from 256 MiB all three within 1 %.
+constexpr int kBulkFanTile = 8192;
+constexpr int64_t kBulkFanWaitNs = 2000000000LL;
+
+__global__ void __launch_bounds__(32) k_fanout_bulk(const __grid_constant__ FanoutArgs a) {
+  __shared__ __align__(128) unsigned char buf[kBulkFanTile];
+  __shared__ __align__(8) uint64_t full;
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x;
+  const int j = blockIdx.y;
+  const char* src = a.src[j];
+  const int64_t nb = a.nbytes;
+  const int64_t head = min(nb, static_cast<int64_t>((16u - (reinterpret_cast<uintptr_t>(src) & 15u)) & 15u));
+  const int64_t body = (nb - head) & ~static_cast<int64_t>(15);
+  if (blockIdx.x == 0) {
+    for (int64_t b = lane; b < nb - body; b += 32) {
+      const int64_t x = b < head ? b : body + b;
+      const char v = src[x];
+      for (int q = 0; q < a.ndst; ++q) a.dst[q][a.job_off[j] + x] = v;
+    }
+  }
+  const uint32_t bar = smem_addr(&full);
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  uint32_t phase = 0;
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kBulkFanTile; t0 < body;
+       t0 += static_cast<int64_t>(gridDim.x) * kBulkFanTile, phase ^= 1u) {
+    const uint32_t len = static_cast<uint32_t>(min(static_cast<int64_t>(kBulkFanTile), body - t0));
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, len);
+      bulk_load(smem_addr(buf), src + head + t0, len, bar);
+    }
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar, phase, kBulkFanWaitNs))) {
+      if (lane == 0 && a.err) atomicCAS(a.err, 0, kErrBulkWait);
+      (void)mbar_wait_bounded(bar, phase, kBulkFanWaitNs);  // the load must land before shared memory goes away
+      return;
+    }
+    for (int q = lane; q < a.ndst; q += 32) bulk_store(a.dst[q] + a.job_off[j] + head + t0, smem_addr(buf), len);
+    bulk_commit();
+    bulk_wait_read(0);  // the tile has been read out before the next load overwrites it
+    __syncwarp();
+  }
+  bulk_wait_all();  // this lane's stores are complete
 }
 
 __device__ __forceinline__ int find_tile_owner(const int32_t* tile0, int nseg, int32_t b) {
@@ -219,10 +282,41 @@ cudaError_t launch_pair_copy(const PairCopyArgs& a, cudaStream_t s) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s) {
+// Every job's source and every destination of it agree modulo 16 bytes.
+bool fanout_aligned(const FanoutArgs& a) {
+  for (int j = 0; j < a.njobs; ++j)
+    for (int q = 0; q < a.ndst; ++q)
+      if (((reinterpret_cast<uintptr_t>(a.dst[q]) + static_cast<uintptr_t>(a.job_off[j])) ^
+           reinterpret_cast<uintptr_t>(a.src[j])) & 15u)
+        return false;
+  return true;
+}
+
+// Which fan-out DDP_ALGO_FUSED takes: the bulk-copy form with 7 or more
+// destinations once the job reads 64 MiB or more in all, where it measured
+// faster on GB300 (broadcast / all-gather, fraction of measured HBM, bulk
+// against registers: p = 8 at 256 MiB 1.002 / 1.002 against 0.991 / 0.989,
+// at 1 GiB 1.004 / 1.003 against 0.997 / 0.994; p = 16 at 64 MiB 1.003 /
+// 1.007 against 0.980 / 0.979, at 256 MiB 1.016 / 1.016 against 0.978 /
+// 0.982; p = 64 at 64 MiB 1.037 / 1.036 against 1.012 / 1.012, at 256 MiB
+// 1.061 / 1.054 against 1.025 / 1.013). With fewer destinations, or below
+// 64 MiB where its grid holds too few blocks, the register form was faster
+// (p = 2 at 1 GiB: 1.034 against 1.046; p = 8 at 16 MiB with 16 KB tiles:
+// 0.73 against 0.91).
+bool fanout_bulk_by_default(const FanoutArgs& a) {
+  return a.ndst >= 7 && static_cast<int64_t>(a.njobs) * a.nbytes >= (int64_t(64) << 20);
+}
+
+cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s, ddp_algo algo) {
   if (a.njobs <= 0 || a.nbytes <= 0 || a.ndst <= 0) return cudaSuccess;
   cudaError_t e;
-  if (a.ndst <= kFanFewDst) {
+  const bool bulk = algo == DDP_ALGO_FUSED_TMA || (algo == DDP_ALGO_FUSED && fanout_bulk_by_default(a));
+  if (bulk && fanout_aligned(a)) {
+    FanoutArgs b = a;
+    b.err = device_error_word();
+    e = launch_pdl(k_fanout_bulk, dim3(grid_x_for((a.nbytes + kBulkFanTile - 1) / kBulkFanTile), a.njobs),
+                   dim3(32), 0, s, b);
+  } else if (a.ndst <= kFanFewDst) {
     constexpr int64_t t = fan_tile_bytes<4>();
     e = launch_pdl(k_fanout<4>, dim3(grid_x_for((a.nbytes + t - 1) / t), a.njobs), dim3(kThreads), 0, s, a);
   } else {

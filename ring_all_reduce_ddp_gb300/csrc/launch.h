@@ -25,7 +25,11 @@ cudaError_t launch_ring_persistent(const PersistArgs& a, cudaStream_t s);
 int ring_persistent_max_blocks();  // co-resident blocks of the persistent ring kernel on this device
 cudaError_t launch_pair_copy(const PairCopyArgs& a, cudaStream_t s);
 cudaError_t launch_pair_add(const PairAddArgs& a, cudaStream_t s);
-cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s);
+// algo: DDP_ALGO_FUSED_TMA the TMA bulk-copy form (k_fanout_bulk) when every
+// source and destination agree modulo 16 bytes, DDP_ALGO_FUSED_LDST the
+// register form (k_fanout), DDP_ALGO_FUSED whichever measured faster for the
+// destination count and size.
+cudaError_t launch_fanout(const FanoutArgs& a, cudaStream_t s, ddp_algo algo = DDP_ALGO_FUSED_LDST);
 cudaError_t launch_seg_copy(const SegCopyArgs& a, ddp_dtype dt, cudaStream_t s);
 cudaError_t launch_multi_fanout(const MultiFanoutArgs& a, cudaStream_t s);
 cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t s);

@@ -235,3 +235,32 @@ def test_kernel_launch_counter_counts():
     D.ddp_allreduce(devs, 1000, D.DDP_FLOAT32, 8.0, D.DDP_ALGO_FUSED)
     D.ddp_allreduce(devs, 1000, D.DDP_FLOAT32, 8.0, D.DDP_ALGO_RING_STEPS)
     assert D.ddp_kernel_launches() - before == 1 + 2 * 7
+
+
+@pytest.mark.parametrize("algo", [D.DDP_ALGO_FUSED, D.DDP_ALGO_FUSED_TMA])
+def test_large_fanouts_by_bulk_copies(algo):
+    """Fan-outs large enough that DDP_ALGO_FUSED takes the bulk-copy form
+    (7 or more destinations, 64 MiB or more read): a broadcast of 64 MiB plus
+    a ragged 1,007 bytes whose replicas all start 4 bytes past a 16-byte
+    boundary (12 bytes before the first boundary go singly, as does the
+    tail), and an all-gather of 8 replicas' 2,097,156-element fp32 chunks.
+    Against the oracle's copies, byte for byte."""
+    p, root = 8, 5
+    nbytes = (64 << 20) + 1007
+    gen = torch.Generator().manual_seed(77)
+    host = [torch.randint(0, 256, (nbytes + 4,), dtype=torch.uint8, generator=gen) for _ in range(p)]
+    devs = [h.cuda() for h in host]
+    views = [d[4:4 + nbytes] for d in devs]
+    D.ddp_broadcast(views, nbytes, root, algo)
+    want, _, _ = orc.broadcast_tree([h[4:4 + nbytes].numpy() for h in host], root)
+    for r in range(p):
+        assert np.array_equal(views[r].cpu().numpy(), want[r]), r
+        assert np.array_equal(devs[r][:4].cpu().numpy(), host[r][:4].numpy())
+    m = 2097156
+    ins, hosts, _ = make_replicas(p, m, "f32", "uniform", seed=401)
+    outs = [torch.zeros(p * m, dtype=torch.float32, device="cuda") for _ in range(p)]
+    D.ddp_allgather(ins, outs, m, D.DDP_FLOAT32, D.DDP_OWN_RANK, algo)
+    want, _ = orc.allgather(hosts, "f32", "rank")
+    for r in range(p):
+        assert_bit_equal(to_host(outs[r]), want[r], f"rank {r}")
+    assert D.ddp_device_error() == 0

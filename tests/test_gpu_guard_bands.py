@@ -98,7 +98,7 @@ def test_reduce_scatter_small_sizes_stay_inside(own, algo):
                 assert gs[r].margins_intact() and _eq(_host(gs[r], "f32"), hosts[r]), (p, n, r)
 
 
-@pytest.mark.parametrize("algo", [D.DDP_ALGO_FUSED, D.DDP_ALGO_RING_STEPS])
+@pytest.mark.parametrize("algo", [D.DDP_ALGO_FUSED, D.DDP_ALGO_FUSED_TMA, D.DDP_ALGO_RING_STEPS])
 def test_allgather_and_broadcast_small_sizes_stay_inside(algo):
     for p in PS:
         for m in range(0, 12):
