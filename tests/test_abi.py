@@ -165,3 +165,18 @@ def test_c_program_compiles_against_the_header_alone(L, tmp_path):
            "-o", str(tmp_path / "abi_smoke")]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    """include/ddp_ring.h is a C header: it compiles as C99 (only the CUDA
+    runtime's stream type is needed from outside)."""
+    import shutil
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if gcc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers are not available")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "ddp_ring.h"\nint main(void) { return ddp_reducer_staged(0) == -1 ? 0 : 1; }\n')
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
