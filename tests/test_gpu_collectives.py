@@ -264,3 +264,26 @@ def test_large_fanouts_by_bulk_copies(algo):
     for r in range(p):
         assert_bit_equal(to_host(outs[r]), want[r], f"rank {r}")
     assert D.ddp_device_error() == 0
+
+
+@pytest.mark.parametrize("p", [33, 64, 256])
+def test_bulk_fanout_with_more_destinations_than_lanes(p):
+    """The bulk-copy fan-out's warp issues one store per destination, lane q
+    taking destinations q, q + 32, ...: broadcasts and all-gathers to 32 or
+    more replicas, aligned so that the bulk form runs, with a ragged tail."""
+    nbytes = 3 * 8192 + 48 + 5
+    gen = torch.Generator().manual_seed(p)
+    host = [torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=gen) for _ in range(p)]
+    devs = [h.cuda() for h in host]
+    D.ddp_broadcast(devs, nbytes, p - 1, D.DDP_ALGO_FUSED_TMA)
+    want, _, _ = orc.broadcast_tree([h.numpy() for h in host], p - 1)
+    for r in range(p):
+        assert np.array_equal(devs[r].cpu().numpy(), want[r]), r
+    m = 2052  # 8,208 bytes per chunk: every job offset stays 16-byte aligned
+    ins, hosts, _ = make_replicas(p, m, "f32", "uniform", seed=500 + p)
+    outs = [torch.zeros(p * m, dtype=torch.float32, device="cuda") for _ in range(p)]
+    D.ddp_allgather(ins, outs, m, D.DDP_FLOAT32, D.DDP_OWN_RING, D.DDP_ALGO_FUSED_TMA)
+    want, _ = orc.allgather(hosts, "f32", "ring")
+    for r in range(p):
+        assert_bit_equal(to_host(outs[r]), want[r], f"rank {r}")
+    assert D.ddp_device_error() == 0
